@@ -1,0 +1,227 @@
+// attention_oracle.cpp -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, fp64 CPU statement of what the fused attention path computes.  It is the
+// parity oracle for the CUDA library and shares no code with it.  Only the test suite, the
+// package's smoke check and the benchmark's CPU-baseline leg may load it.
+//
+// Every function is written from the definitions on the pages it cites:
+//   [FA-GEM]  "Flash Attention: The Hidden Gem" (ashishkpokharel.com.np/blogs/flash-attention)
+//   [FA-IO]   "FlashAttention: attention was never compute-bound" (paperfordummies.in)
+//   [FA-UND]  "Understanding FlashAttention" (jimwang99.github.io)
+//
+// Arithmetic is fp64 throughout, sums are sequential in key order, and fused multiply-add
+// contraction is disabled at build time so the results are the same on every host.
+//
+// Parity status: every exported function is pinned by tests that do not call back into this
+// file's arithmetic (closed forms, printed values from [FA-IO] demo 2, a 50-digit brute force,
+// and independent restatements of the per-key and tiled recurrences).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+const double kNegInf = -std::numeric_limits<double>::infinity();
+
+// Causal visibility, bottom-right aligned: query row i of Nq may see key j of Nk iff
+// j <= i + (Nk - Nq).  With Nq == Nk this is the usual lower triangle j <= i.  The pages only
+// say "causal masking ... is an elementwise operation" ([FA-UND] "Attention") and use
+// is_causal=True ([FA-GEM] opening code); the alignment for Nq != Nk is this file's reading.
+inline bool visible(int64_t i, int64_t j, int64_t Nq, int64_t Nk, int causal) {
+    if (!causal) return true;
+    return j <= i + (Nk - Nq);
+}
+
+// One query row of the attention definition, three logical passes as in safe softmax
+// ([FA-GEM] "Safe Softmax" and "Why is Flash Attention needed?"; [FA-UND] "Safe softmax"):
+//   x_j = scale * <q, k_j>            for every visible key j
+//   m   = max_j x_j                   (pass 1)
+//   l   = sum_j exp(x_j - m)          (pass 2)
+//   o   = sum_j exp(x_j - m) / l * v_j  (pass 3)
+//   lse = m + log(l)                  ([FA-GEM] step 6: L = m + log(l))
+// Masked keys are excluded outright (their weight is exactly zero).  Returns the number of
+// visible keys; with none visible the row is left as NaN (the pages: -inf minus -inf is
+// undefined, [FA-UND] "What is left to the implementation").
+int64_t attention_row(const double* q, const double* k, const double* v, int64_t i, int64_t Nq,
+                      int64_t Nk, int64_t d, int causal, double scale, double* x_scratch,
+                      double* o, double* lse) {
+    int64_t nvis = 0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        if (!visible(i, j, Nq, Nk, causal)) {
+            x_scratch[j] = kNegInf;
+            continue;
+        }
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t) dot += q[t] * k[j * d + t];
+        x_scratch[j] = scale * dot;
+        ++nvis;
+    }
+    if (nvis == 0) {
+        for (int64_t t = 0; t < d; ++t) o[t] = std::numeric_limits<double>::quiet_NaN();
+        *lse = std::numeric_limits<double>::quiet_NaN();
+        return 0;
+    }
+    double m = kNegInf;  // pass 1
+    for (int64_t j = 0; j < Nk; ++j) m = std::max(m, x_scratch[j]);
+    double l = 0.0;  // pass 2
+    for (int64_t j = 0; j < Nk; ++j)
+        if (x_scratch[j] != kNegInf) l += std::exp(x_scratch[j] - m);
+    for (int64_t t = 0; t < d; ++t) o[t] = 0.0;  // pass 3
+    for (int64_t j = 0; j < Nk; ++j) {
+        if (x_scratch[j] == kNegInf) continue;
+        const double p = std::exp(x_scratch[j] - m) / l;
+        for (int64_t t = 0; t < d; ++t) o[t] += p * v[j * d + t];
+    }
+    *lse = m + std::log(l);
+    return nvis;
+}
+
+template <class F>
+void parallel_for(int64_t n, int nthreads, F&& f) {
+    if (nthreads <= 1 || n <= 1) {
+        for (int64_t r = 0; r < n; ++r) f(r);
+        return;
+    }
+    const int T = static_cast<int>(std::min<int64_t>(nthreads, n));
+    std::vector<std::thread> pool;
+    pool.reserve(T);
+    for (int w = 0; w < T; ++w) {
+        pool.emplace_back([&, w]() {
+            for (int64_t r = w; r < n; r += T) f(r);
+        });
+    }
+    for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Safe softmax over one vector, three logical passes ([FA-GEM] "Safe Softmax";
+// [FA-UND] "Safe softmax"): max, then the exp-sum, then the division.
+void oracle_softmax(const double* x, int64_t n, double* y) {
+    double m = kNegInf;
+    for (int64_t j = 0; j < n; ++j) m = std::max(m, x[j]);
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) l += std::exp(x[j] - m);
+    for (int64_t j = 0; j < n; ++j) y[j] = std::exp(x[j] - m) / l;
+}
+
+// Online softmax streamed block by block ([FA-IO] "The one formula" and "Online softmax: the
+// whole idea"; [FA-GEM] "Online Softmax").  A running max m and running sum l are carried over
+// blocks of `block` scores; when a block raises the max, the old sum is multiplied by
+// exp(m_old - m_new) before the block's terms exp(x - m_new) are added.  With rescale == 0 that
+// multiplication is dropped, which is the deliberately broken variant the page uses to show
+// that the correction is load-bearing.  The output vector is exp(x - m_final) / l_final.
+void oracle_online_softmax(const double* x, int64_t n, int64_t block, int rescale, double* y) {
+    double m = kNegInf;
+    double l = 0.0;
+    for (int64_t j0 = 0; j0 < n; j0 += block) {
+        const int64_t j1 = std::min(n, j0 + block);
+        double m_new = m;
+        for (int64_t j = j0; j < j1; ++j) m_new = std::max(m_new, x[j]);
+        if (rescale && m != kNegInf) l = l * std::exp(m - m_new);
+        for (int64_t j = j0; j < j1; ++j) l += std::exp(x[j] - m_new);
+        m = m_new;
+    }
+    for (int64_t j = 0; j < n; ++j) y[j] = std::exp(x[j] - m) / l;
+}
+
+// The per-element online normalizer ([FA-UND] "Online softmax"; Milakov & Gimelshein as cited
+// there): g_i = max(g_{i-1}, x_i), s_i = s_{i-1} * exp(g_{i-1} - g_i) + exp(x_i - g_i), started
+// from g_1 = x_1, s_1 = 1.  Writes the final pair (g_N, s_N).
+void oracle_online_normalizer(const double* x, int64_t n, double* g_out, double* s_out) {
+    if (n <= 0) {
+        *g_out = kNegInf;
+        *s_out = 0.0;
+        return;
+    }
+    double g = x[0];
+    double s = 1.0;
+    for (int64_t i = 1; i < n; ++i) {
+        const double g_new = std::max(g, x[i]);
+        s = s * std::exp(g - g_new) + std::exp(x[i] - g_new);
+        g = g_new;
+    }
+    *g_out = g;
+    *s_out = s;
+}
+
+// Attention by its definition, O = softmax(scale * Q K^T + mask) V, plus L = m + log(l) per row
+// ([FA-GEM] "Background" and step 6; [FA-UND] "Attention" for the [N,D]/[M,D] shapes and the
+// note that batch and heads only repeat independent problems).
+//   q: [B,H,Nq,d], k,v: [B,H,Nk,d], o: [B,H,Nq,d], lse: [B,H,Nq]; all row-major fp64.
+// Returns the number of rows that had no visible key (0 for every valid causal problem).
+int64_t oracle_attention(const double* q, const double* k, const double* v, double* o, double* lse,
+                         int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                         double scale, int nthreads) {
+    const int64_t rows = B * H * Nq;
+    std::vector<int64_t> empty(static_cast<size_t>(std::max<int64_t>(rows, 1)), 0);
+    parallel_for(rows, nthreads, [&](int64_t r) {
+        thread_local std::vector<double> xs;
+        xs.resize(static_cast<size_t>(Nk));
+        const int64_t bh = r / Nq, i = r % Nq;
+        const int64_t n = attention_row(q + r * d, k + bh * Nk * d, v + bh * Nk * d, i, Nq, Nk, d,
+                                        causal, scale, xs.data(), o + r * d, lse + r);
+        empty[static_cast<size_t>(r)] = (n == 0);
+    });
+    int64_t n_empty = 0;
+    for (int64_t r = 0; r < rows; ++r) n_empty += empty[static_cast<size_t>(r)];
+    return n_empty;
+}
+
+// The same definition for a chosen subset of rows (flat indices into B*H*Nq), so that very
+// large problems can be checked on sampled outputs one row at a time.  Row n of the result is
+// written to o_rows[n*d ...] and lse_rows[n].
+int64_t oracle_attention_rows(const double* q, const double* k, const double* v, const int64_t* rows,
+                              int64_t nrows, double* o_rows, double* lse_rows, int64_t B, int64_t H,
+                              int64_t Nq, int64_t Nk, int64_t d, int causal, double scale,
+                              int nthreads) {
+    (void)B;
+    (void)H;
+    std::vector<int64_t> empty(static_cast<size_t>(std::max<int64_t>(nrows, 1)), 0);
+    parallel_for(nrows, nthreads, [&](int64_t n) {
+        thread_local std::vector<double> xs;
+        xs.resize(static_cast<size_t>(Nk));
+        const int64_t r = rows[n];
+        const int64_t bh = r / Nq, i = r % Nq;
+        const int64_t cnt = attention_row(q + r * d, k + bh * Nk * d, v + bh * Nk * d, i, Nq, Nk, d,
+                                          causal, scale, xs.data(), o_rows + n * d, lse_rows + n);
+        empty[static_cast<size_t>(n)] = (cnt == 0);
+    });
+    int64_t n_empty = 0;
+    for (int64_t n = 0; n < nrows; ++n) n_empty += empty[static_cast<size_t>(n)];
+    return n_empty;
+}
+
+// The probability matrix of one head, P = softmax(scale * Q K^T + mask), row by row with the
+// same three passes ([FA-GEM] "Why is Flash Attention needed?", steps 1-2).  p: [Nq, Nk];
+// masked entries are exactly 0.
+void oracle_attention_probs(const double* q, const double* k, int64_t Nq, int64_t Nk, int64_t d,
+                            int causal, double scale, double* p) {
+    std::vector<double> xs(static_cast<size_t>(Nk));
+    for (int64_t i = 0; i < Nq; ++i) {
+        double m = kNegInf;
+        for (int64_t j = 0; j < Nk; ++j) {
+            if (!visible(i, j, Nq, Nk, causal)) {
+                xs[j] = kNegInf;
+                continue;
+            }
+            double dot = 0.0;
+            for (int64_t t = 0; t < d; ++t) dot += q[i * d + t] * k[j * d + t];
+            xs[j] = scale * dot;
+            m = std::max(m, xs[j]);
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < Nk; ++j)
+            if (xs[j] != kNegInf) l += std::exp(xs[j] - m);
+        for (int64_t j = 0; j < Nk; ++j)
+            p[i * Nk + j] = (xs[j] == kNegInf) ? 0.0 : std::exp(xs[j] - m) / l;
+    }
+}
+
+}  // extern "C"
