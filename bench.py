@@ -1,0 +1,598 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step is one pass of the whole path over one batch of synthetic input:
+  1. the fused causal prefill forward, B=1, H=32, Nq=Nk=8192, d=64 (fattn_fwd), and
+  2. one split-KV decode, B=32, H=32, Nq=1, Nk=16384, d=128 (fattn_decode: split + combine).
+`value` is the prefill throughput in TFLOP/s (4*B*H*Nq*Nk*d, halved for causal) from CUDA events
+around each prefill launch; the decode's KV-read bandwidth is reported beside it.  Before every
+timed prefill the L2 is flushed by writing a 512 MiB buffer (the prefill inputs are smaller than
+L2); the decode reads 8 GiB, which no cache holds.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, no data-path
+collective); the timed region is bracketed by a barrier and a device synchronize, the time is the
+maximum over ranks, and rank 0 prints one JSON line.  `--impl reference` times the fp64 CPU oracle
+on this host's cores on a bounded sample of the same workload (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; decode KV GB/s vs HBM peak"
+PREFILL = dict(name="prefill_b1h32_n8192_d64", B=1, H=32, N=8192, d=64, causal=True)
+DECODE = dict(name="decode_b32h32_nk16384_d128", B=32, H=32, Nk=16384, d=128)
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PREFILL_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "prefill_sm103a.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "decode_sm103a.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+# ------------------------------------------------------------------------------------------------
+# Algorithmic work per launch
+# ------------------------------------------------------------------------------------------------
+def prefill_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def prefill_bytes(B, H, N, d):
+    # read Q, K, V once, write O (bf16) and L (fp32)
+    return B * H * N * d * 2 * 4 + B * H * N * 4
+
+
+def decode_kv_bytes(B, H, Nk, d):
+    return 2 * B * H * Nk * d * 2
+
+
+def decode_bytes(B, H, Nk, d):
+    # K and V once, q in, O out (bf16), L out (fp32)
+    return decode_kv_bytes(B, H, Nk, d) + 2 * B * H * d * 2 + B * H * 4
+
+
+# ------------------------------------------------------------------------------------------------
+# Peaks, traffic evidence, clocks
+# ------------------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel source has
+    changed since the counters were taken.  Lines: `<kernel> <source-sha16> <bytes_per_launch>`."""
+    src = {"prefill": PREFILL_KERNEL_SRC, "decode": DECODE_KERNEL_SRC}[kernel]
+    try:
+        digest = source_digest(src)
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == kernel and not line.startswith("#"):
+                    return float(parts[2]) if parts[1] == digest else None
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; samples carry host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        return summarize_clocks(self.samples, t0, t1)
+
+
+def summarize_clocks(samples, t0, t1):
+    inside = [s for t, s in samples if t0 <= t <= t1]
+    note = "samples inside the timed region"
+    if not inside and samples:
+        mid = 0.5 * (t0 + t1)
+        inside = [min(samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        note = "timed region shorter than the sampling interval: nearest sample"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+
+    sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+    mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+    reasons = set()
+    for s in inside:
+        for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), s[5:9]):
+            if val.strip().lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------------------------------------------
+# Distributed plumbing (replicas only)
+# ------------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x, dist, device):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline figure)
+# ------------------------------------------------------------------------------------------------
+def oracle_prefill_sample(q, k, v, budget_s, seed=0):
+    """Time the oracle on random query rows of the prefill workload until `budget_s` has passed.
+    Returns (flops_done, seconds, rows_done, threads)."""
+    import numpy as np
+    import oracle
+    B, H, N, d = q.shape
+    qq = q.reshape(B * H, N, d)
+    rng = np.random.default_rng(seed)
+    threads = oracle.default_threads()
+    flops = 0.0
+    rows_done = 0
+    t_total = 0.0
+    while t_total < budget_s:
+        bh = int(rng.integers(0, B * H))
+        rows = np.sort(rng.choice(N, size=min(N, 64 * threads), replace=False))
+        qf = np.zeros((1, 1, N, d))
+        qf[0, 0, rows] = qq[bh, rows]
+        kf = k.reshape(B * H, N, d)[bh][None, None]
+        vf = v.reshape(B * H, N, d)[bh][None, None]
+        t0 = time.perf_counter()
+        oracle.attention_rows(qf, kf, vf, rows, causal=True, scale=1 / math.sqrt(d), nthreads=threads)
+        t_total += time.perf_counter() - t0
+        flops += float(np.sum(4.0 * (rows + 1) * d))  # row i sees i + 1 keys
+        rows_done += rows.size
+    return flops, t_total, rows_done, threads
+
+
+def oracle_decode_sample(q, k, v, budget_s, seed=1):
+    """Time the oracle on (b, h) pairs of the decode workload; returns (kv_bytes, s, pairs, threads)."""
+    import numpy as np
+    import oracle
+    B, H, Nk, d = k.shape
+    rng = np.random.default_rng(seed)
+    threads = oracle.default_threads()
+    done = 0
+    t_total = 0.0
+    while t_total < budget_s and done < B * H:
+        b, h = int(rng.integers(0, B)), int(rng.integers(0, H))
+        qq, kk, vv = q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1]
+        t0 = time.perf_counter()
+        oracle.attention(qq, kk, vv, causal=False, scale=1 / math.sqrt(d), nthreads=threads)
+        t_total += time.perf_counter() - t0
+        done += 1
+    return float(done * Nk * d * 2 * 2), t_total, done, threads
+
+
+def host_inputs_f64(seed_prefill=0xFA77E004, seed_decode_pairs=0xFA77E005):
+    """Seeded inputs for the CPU timing, drawn on the CPU (same recipe as the GPU inputs)."""
+    import torch
+    from exact_attention_31_gb300.workloads import make_qkv
+    P, D = PREFILL, DECODE
+    q, k, v, _ = make_qkv(P["B"], P["H"], P["N"], P["N"], P["d"], seed_prefill, "cpu")
+    pf = [t.to(torch.float64).numpy() for t in (q, k, v)]
+    # the decode sample needs only a few (b, h) pairs: draw a 2 x 2 slice of the same shape recipe
+    q2, k2, v2, _ = make_qkv(2, 2, 1, D["Nk"], D["d"], seed_decode_pairs, "cpu")
+    df = [t.to(torch.float64).numpy() for t in (q2, k2, v2)]
+    return pf, df
+
+
+def cpu_baseline(budget_s=12.0):
+    pf, df = host_inputs_f64()
+    flops, secs, rows, threads = oracle_prefill_sample(*pf, budget_s=budget_s * 0.75)
+    kvb, dsecs, pairs, _ = oracle_decode_sample(*df, budget_s=budget_s * 0.25)
+    return {
+        "value": flops / secs / 1e12,
+        "unit": "TFLOP/s",
+        "cores": threads,
+        "kind": "oracle",
+        "sample": (f"{rows} random query rows of the causal B1 H32 N8192 d64 prefill ({flops / 1e9:.2f} "
+                   f"GFLOP in {secs:.1f} s); decode: {pairs} (b,h) pairs of Nk=16384 d=128"),
+        "decode_gbs": kvb / dsecs / 1e9,
+    }
+
+
+# ------------------------------------------------------------------------------------------------
+# The GPU arm
+# ------------------------------------------------------------------------------------------------
+def gpu_id_for_smi(dev):
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    return ids[dev.index] if dev.index < len(ids) else dev.index
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_31_gb300 as fa
+    from exact_attention_31_gb300.workloads import make_qkv
+    fa.lib()
+
+    P = dict(PREFILL, H=args.prefill_heads or PREFILL["H"])
+    D = dict(DECODE, B=args.decode_batch or DECODE["B"])
+    do_prefill = args.workload in ("both", "prefill")
+    do_decode = args.workload in ("both", "decode")
+    seed = 0xFA77E000
+    stream = torch.cuda.current_stream(dev)
+    scale_p, scale_d = 1 / math.sqrt(P["d"]), 1 / math.sqrt(D["d"])
+    if do_prefill:
+        q, k, v, _ = make_qkv(P["B"], P["H"], P["N"], P["N"], P["d"], seed + 4, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device=dev)
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if do_decode:
+        dq, dk, dv, _ = make_qkv(D["B"], D["H"], 1, D["Nk"], D["d"], seed + 5, dev)
+        do = torch.empty_like(dq)
+        dlse = torch.empty((D["B"], D["H"], 1), dtype=torch.float32, device=dev)
+        ws = torch.empty(fa.fattn_decode_workspace_size(D["B"], D["H"], D["Nk"], D["d"], 0),
+                         dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if do_prefill:
+            flush.zero_()
+            if evs is not None:
+                evs[0].record(stream)
+            fa.fattn_fwd(q, k, v, causal=True, scale=scale_p, out=o, lse=lse, stream=stream)
+            if evs is not None:
+                evs[1].record(stream)
+        if do_decode:
+            if evs is not None:
+                evs[2].record(stream)
+            fa.fattn_decode(dq, dk, dv, scale=scale_d, num_splits=0, workspace=ws, out=do, lse=dlse,
+                            stream=stream)
+            if evs is not None:
+                evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for_smi(dev)).start() if args.clocks else None
+    if sampler is not None:
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    if sampler is not None:
+        time.sleep(0.15)
+        sampler.stop()
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    pre_avg = dec_avg = None
+    if do_prefill:
+        pre_avg = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, dist, dev)
+    if do_decode:
+        dec_avg = max_over_ranks(sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps, dist, dev)
+
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(fa, dev, stream, args, q if do_prefill else None, k if do_prefill else None,
+                      v if do_prefill else None, dq if do_decode else None, dk if do_decode else None,
+                      dv if do_decode else None, scale_p, scale_d)
+        if do_prefill:
+            e2e["prefill_s"] = max_over_ranks(e2e["prefill_s"], dist, dev)
+        if do_decode:
+            e2e["decode_s"] = max_over_ranks(e2e["decode_s"], dist, dev)
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    pf = prefill_flops(P["B"], P["H"], P["N"], P["d"], True)
+    kv = decode_kv_bytes(D["B"], D["H"], D["Nk"], D["d"])
+    line = {"metric": METRIC}
+    if do_prefill:
+        line.update(value=round(world * pf / (pre_avg * 1e-3) / 1e12, 2), unit="TFLOP/s")
+    else:
+        line.update(value=round(world * kv / (dec_avg * 1e-3) / 1e9, 1), unit="GB/s")
+    name_p = f"prefill_b{P['B']}h{P['H']}_n{P['N']}_d{P['d']} causal"
+    name_d = f"decode_b{D['B']}h{D['H']}_nk{D['Nk']}_d{D['d']}"
+    workload = " + ".join(([name_p] if do_prefill else []) + ([name_d] if do_decode else []))
+    line.update({
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded iid N(0,1) drawn in fp32 and rounded to bf16",
+        "config": {
+            "workload": workload,
+            "l2": ("prefill inputs (96 MiB) are below L2, so a 512 MiB buffer is written before every "
+                   "prefill (inside ms_per_step, outside the per-kernel events); the decode reads 8 GiB"),
+            "parallelism": f"replicas x{world}",
+        },
+    })
+    if do_prefill:
+        per_launch = pf / (pre_avg * 1e-3) / 1e12
+        line["config"]["prefill"] = {"B": P["B"], "H": P["H"], "Nq": P["N"], "Nk": P["N"], "d": P["d"],
+                                     "causal": True, "scale": scale_p, "flops_per_launch": pf}
+        line["prefill_ms"] = round(pre_avg, 4)
+        line["roofline"] = {
+            "kernel": "prefill_kernel<64> (fattn_fwd)",
+            "bound": "tensor", "achieved": round(per_launch, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(per_launch / peaks["bf16_tflops"], 4),
+            "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM)",
+            "traffic": recorded_traffic("prefill"),
+            "algorithmic_bytes": prefill_bytes(P["B"], P["H"], P["N"], P["d"]),
+        }
+    if do_decode:
+        dec_bw = decode_bytes(D["B"], D["H"], D["Nk"], D["d"]) / (dec_avg * 1e-3) / 1e9
+        line["config"]["decode"] = {"B": D["B"], "H": D["H"], "Nq": 1, "Nk": D["Nk"], "d": D["d"],
+                                    "causal": False, "num_splits": fa.fattn_decode_num_splits(D["Nk"], 0),
+                                    "partial_states": "one (m, l, O) per 64-key block",
+                                    "kv_bytes_per_launch": kv}
+        line["decode"] = {"value": round(world * kv / (dec_avg * 1e-3) / 1e9, 1), "unit": "GB/s",
+                          "ms": round(dec_avg, 4), "frac_of_hbm": round(dec_bw / peaks["hbm_gbs"], 4)}
+        rd = {
+            "kernel": "decode_split_kernel<128> + decode_combine_kernel<128> (fattn_decode)",
+            "bound": "hbm", "achieved": round(dec_bw, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(dec_bw / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} copy bandwidth",
+            "traffic": recorded_traffic("decode"),
+            "algorithmic_bytes": decode_bytes(D["B"], D["H"], D["Nk"], D["d"]),
+        }
+        line["roofline_decode" if do_prefill else "roofline"] = rd
+    if args.cpu_budget > 0:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    if e2e is not None:
+        if do_prefill:
+            line["e2e"] = {"value": round(world * pf / e2e["prefill_s"] / 1e12, 3), "unit": "TFLOP/s"}
+        else:
+            line["e2e"] = {"value": round(world * kv / e2e["decode_s"] / 1e9, 1), "unit": "GB/s"}
+        line["e2e"].update({"h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]})
+        if do_prefill and do_decode:
+            line["e2e"]["decode_gbs"] = round(world * kv / e2e["decode_s"] / 1e9, 1)
+        line["e2e"]["how"] = ("the library calls fed from pinned host buffers: H2D of the inputs, the "
+                              "call, D2H of O and L, every step, timed with CUDA events")
+    line["gpu_launches"] = (int(do_prefill) + 2 * int(do_decode)) * args.steps
+    line["clocks"] = sampler.summary(t0, t1) if sampler is not None else None
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(fa, dev, stream, args, q, k, v, dq, dk, dv, scale_p, scale_d):
+    """The same calls fed from pinned host buffers, copies included in the timing."""
+    import torch
+    steps = max(1, min(args.steps, args.e2e_steps))
+    out = {"h2d": 0, "d2h": 0}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if q is not None:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+        def prefill_once():
+            gq.copy_(hq, non_blocking=True)
+            gk.copy_(hk, non_blocking=True)
+            gv.copy_(hv, non_blocking=True)
+            fa.fattn_fwd(gq, gk, gv, causal=True, scale=scale_p, out=o, lse=lse, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        prefill_once()
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(steps):
+            prefill_once()
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        out["prefill_s"] = ev[0].elapsed_time(ev[1]) * 1e-3 / steps
+        out["h2d"] += sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        out["d2h"] += sum(t.numel() * t.element_size() for t in (ho, hl))
+        del hq, hk, hv, gq, gk, gv
+    if dq is not None:
+        hdq, hdk, hdv = (t.cpu().pin_memory() for t in (dq, dk, dv))
+        hdo = torch.empty(dq.shape, dtype=torch.bfloat16).pin_memory()
+        hdl = torch.empty(dq.shape[:3], dtype=torch.float32).pin_memory()
+        gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+        go, gl = torch.empty_like(dq), torch.empty(dq.shape[:3], dtype=torch.float32, device=dev)
+        ws = torch.empty(fa.fattn_decode_workspace_size(dk.shape[0], dk.shape[1], dk.shape[2], dk.shape[3], 0),
+                         dtype=torch.uint8, device=dev)
+
+        def decode_once():
+            gq.copy_(hdq, non_blocking=True)
+            gk.copy_(hdk, non_blocking=True)
+            gv.copy_(hdv, non_blocking=True)
+            fa.fattn_decode(gq, gk, gv, scale=scale_d, workspace=ws, out=go, lse=gl, stream=stream)
+            hdo.copy_(go, non_blocking=True)
+            hdl.copy_(gl, non_blocking=True)
+
+        decode_once()
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(steps):
+            decode_once()
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        out["decode_s"] = ev[0].elapsed_time(ev[1]) * 1e-3 / steps
+        out["h2d"] += sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+        out["d2h"] += sum(t.numel() * t.element_size() for t in (hdo, hdl))
+    return out
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle as it stands, on this host's cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    pf, _ = host_inputs_f64()
+    P = PREFILL
+    budget = max(1.0, args.ref_budget)
+    per_step = budget / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        oracle_prefill_sample(*pf, budget_s=per_step, seed=99)
+    flops = secs = 0.0
+    rows = 0
+    threads = 1
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        f, s_, r, threads = oracle_prefill_sample(*pf, budget_s=per_step, seed=i)
+        flops += f
+        secs += s_
+        rows += r
+    t_wall = time.perf_counter() - t_wall
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t_wall / max(1, args.steps), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: seeded iid N(0,1) drawn in fp32 and rounded to bf16, computed in fp64",
+        "config": {"workload": "prefill_b1h32_n8192_d64 causal (sampled rows)",
+                   "prefill": {"B": P["B"], "H": P["H"], "Nq": P["N"], "Nk": P["N"], "d": P["d"],
+                               "causal": True}},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": (f"{rows} random query rows over the run, about {per_step:.1f} s of "
+                                    "oracle work per step")},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description="exact-attention hot-path benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
+                    help="both = the benchmark step; the others time one half (used for profiling)")
+    ap.add_argument("--prefill-heads", type=int, default=0, help="override H of the prefill (profiling)")
+    ap.add_argument("--decode-batch", type=int, default=0, help="override B of the decode (profiling)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline figure (0 = skip)")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="seconds of oracle work for the whole --impl reference run")
+    ap.add_argument("--e2e-steps", type=int, default=5, help="steps of the host-buffer run (0 = skip)")
+    ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+"""exact_attention_31_gb300 -- exact fused attention for GB300 (sm_103a), Python binding.
+
+The compute lives in ``libfattn.so`` (hand-written CUDA: a tcgen05/TMEM/TMA prefill kernel, and a
+split-KV decode kernel with its combine kernel) behind the C ABI in ``include/fattn.h``.  This
+module only marshals torch tensors into that ABI: it checks dtypes, devices and shapes, allocates
+outputs with torch when the caller does not pass them, and raises on a non-OK status.  There is no
+other implementation behind these names: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "FattnError",
+    "fattn_fwd",
+    "fattn_decode",
+    "fattn_decode_num_splits",
+    "fattn_decode_workspace_size",
+    "fattn_last_error",
+    "fattn_status_string",
+    "lib",
+    "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn.so")
+
+FATTN_OK = 0
+FATTN_ERR_INVALID_ARG = 1
+FATTN_ERR_UNSUPPORTED = 2
+FATTN_ERR_CUDA = 3
+FATTN_ERR_TIMEOUT = 4
+
+_lib = None
+
+
+class FattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fattn_status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfattn (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                           "g.build()'` (nvcc, sm_103a); there is no fallback implementation")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.fattn_fwd.restype = i
+    L.fattn_decode_num_splits.argtypes = [i, i]
+    L.fattn_decode_num_splits.restype = i
+    L.fattn_decode_workspace_size.argtypes = [i, i, i, i, i]
+    L.fattn_decode_workspace_size.restype = sz
+    L.fattn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    L.fattn_decode.restype = i
+    L.fattn_last_error.argtypes = [vp]
+    L.fattn_last_error.restype = i
+    L.fattn_status_string.argtypes = [i]
+    L.fattn_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def fattn_status_string(status: int) -> str:
+    try:
+        return lib().fattn_status_string(int(status)).decode()
+    except RuntimeError:
+        return {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
+                3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}.get(int(status), "FATTN_UNKNOWN_STATUS")
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+
+
+def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+              stream=None, want_lse: bool = True):
+    """O = softmax(scale * Q K^T + mask) V and L per row, via the fused sm_103a kernel.
+
+    q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; d in {64, 128}.  Causal masking is bottom-right
+    aligned.  Returns (out bf16 [B,H,Nq,d], lse fp32 [B,H,Nq] or None).
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError(f"expected q [B,H,Nq,d], k/v [B,H,Nk,d]; got {tuple(q.shape)}, {tuple(k.shape)}, {tuple(v.shape)}")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q and k/v disagree on B, H or d")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32)
+    st = lib().fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d,
+                         1 if causal else 0, float(scale), _stream_handle(stream, q.device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_fwd")
+    return out, lse
+
+
+def fattn_decode_num_splits(Nk: int, num_splits: int = 0) -> int:
+    return lib().fattn_decode_num_splits(int(Nk), int(num_splits))
+
+
+def fattn_decode_workspace_size(B: int, H: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    return lib().fattn_decode_workspace_size(int(B), int(H), int(Nk), int(d), int(num_splits))
+
+
+def fattn_decode(q, k_cache, v_cache, scale: float | None = None, num_splits: int = 0, workspace=None,
+                 out=None, lse=None, stream=None, want_lse: bool = True):
+    """One query token per (b, h) against a KV cache, split-KV + combine on the GPU.
+
+    q: bf16 [B,H,1,d]; k_cache, v_cache: bf16 [B,H,Nk,d].  ``workspace`` is a CUDA uint8 tensor of
+    at least fattn_decode_workspace_size(...) bytes (allocated here if omitted).
+    Returns (out bf16 [B,H,1,d], lse fp32 [B,H,1] or None).
+    """
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16)
+    if q.dim() != 4 or q.shape[2] != 1 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected q [B,H,1,d] and k/v caches [B,H,Nk,d]")
+    B, H, _, d = q.shape
+    if k_cache.shape[0] != B or k_cache.shape[1] != H or k_cache.shape[3] != d:
+        raise ValueError("q and the caches disagree on B, H or d")
+    Nk = k_cache.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = fattn_decode_workspace_size(B, H, Nk, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32)
+    st = lib().fattn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, Nk, d, float(scale),
+                            int(num_splits), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream, q.device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_decode")
+    return out, lse
+
+
+def fattn_last_error(stream=None) -> int:
+    """Synchronise ``stream`` and read-and-clear the on-device status word (0 = OK, 4 = timeout)."""
+    import torch
+    return lib().fattn_last_error(_stream_handle(stream, torch.device("cuda", torch.cuda.current_device())))

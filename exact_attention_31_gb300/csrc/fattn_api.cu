@@ -1,0 +1,190 @@
+// fattn_api.cu -- the C ABI of libfattn: argument checks, TMA descriptors, launches, status.
+//
+// Every entry point validates its arguments on the host and launches nothing when they are bad;
+// no entry point allocates device memory.  The declarations and their contracts are in fattn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "fattn.h"
+#include "fattn_internal.h"
+
+namespace fattn {
+namespace {
+
+// Status word the kernels raise bits in (bounded waits that gave up).  One copy per device.
+__device__ unsigned int g_device_status;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+unsigned long long wait_timeout_ns() {
+  static unsigned long long ns = [] {
+    const char* s = getenv("FATTN_WAIT_TIMEOUT_MS");
+    long long ms = s ? atoll(s) : 0;
+    if (ms <= 0) ms = 4000;
+    return static_cast<unsigned long long>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+// Device address of g_device_status for the current device, looked up once per device.
+cudaError_t device_status_ptr(unsigned int** out) {
+  static std::mutex mu;
+  static unsigned int* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && cache[dev] != nullptr) {
+    *out = cache[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_device_status);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned int*>(p);
+  *out = static_cast<unsigned int*>(p);
+  return cudaSuccess;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// [BH][N][d] bf16, 128-row x 64-column boxes, 128-byte swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool positive_sizes(long long a, long long b, long long c, long long d) {
+  return a >= 1 && b >= 1 && c >= 1 && d >= 1;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+}  // namespace fattn
+
+using namespace fattn;
+
+extern "C" {
+
+const char* fattn_status_string(int status) {
+  switch (status) {
+    case FATTN_OK: return "FATTN_OK";
+    case FATTN_ERR_INVALID_ARG: return "FATTN_ERR_INVALID_ARG";
+    case FATTN_ERR_UNSUPPORTED: return "FATTN_ERR_UNSUPPORTED";
+    case FATTN_ERR_CUDA: return "FATTN_ERR_CUDA";
+    case FATTN_ERR_TIMEOUT: return "FATTN_ERR_TIMEOUT";
+    default: return "FATTN_UNKNOWN_STATUS";
+  }
+}
+
+fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                       int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nq, Nk)) return FATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FATTN_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL / 64) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, BH, Nq, d) || !make_map(&tk, k, BH, Nk, d) || !make_map(&tv, v, BH, Nk, d))
+    return FATTN_ERR_CUDA;
+  unsigned int* status = nullptr;
+  if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
+  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale};
+  if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+int fattn_decode_num_splits(int Nk, int num_splits) {
+  if (Nk < 1) return -1;
+  const int nblk = (Nk + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
+  if (num_splits == 0) return nblk;
+  if (num_splits < 0 || num_splits > nblk) return -1;
+  return num_splits;
+}
+
+size_t fattn_decode_workspace_size(int B, int H, int Nk, int d, int num_splits) {
+  if (!positive_sizes(B, H, Nk, d)) return 0;
+  const int S = fattn_decode_num_splits(Nk, num_splits);
+  if (S < 1) return 0;
+  const size_t parts = static_cast<size_t>(B) * H * S;
+  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256);
+}
+
+fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                          int B, int H, int Nk, int d, float scale, int num_splits, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !o || !workspace) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(workspace) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nk, 1)) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const int S = fattn_decode_num_splits(Nk, num_splits);
+  if (S < 1) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * S > 0x7fffffffLL) return FATTN_ERR_INVALID_ARG;
+  const size_t need = fattn_decode_workspace_size(B, H, Nk, d, num_splits);
+  if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+  const size_t parts = static_cast<size_t>(B) * H * S;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align_up(parts * d * sizeof(float), 256));
+  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml};
+  if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+fattn_status fattn_last_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  unsigned int* status = nullptr;
+  if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
+  unsigned int h = 0;
+  if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (h != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FATTN_ERR_CUDA;
+  }
+  return (h & kStatusTimeout) ? FATTN_ERR_TIMEOUT : FATTN_OK;
+}
+
+}  // extern "C"

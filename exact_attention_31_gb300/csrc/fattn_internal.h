@@ -1,0 +1,50 @@
+// fattn_internal.h -- launcher interfaces shared by the host entry points and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "fattn.h"
+
+namespace fattn {
+
+// Status bits the kernels may set in the library's device status word.
+constexpr unsigned int kStatusTimeout = 1u;
+
+struct FwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, Nq, Nk, d, causal;
+  float scale;
+};
+
+struct DecodeProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, Nk, d;
+  float scale;
+  int num_splits;    // resolved, in [1, nblk]
+  float* ws_o;       // [B*H*num_splits, d] partial unnormalised outputs
+  float* ws_ml;      // [B*H*num_splits, 2] partial (m, l), m in log2 units of the scaled score
+};
+
+// Keys per decode block: the unit a split is made of.
+constexpr int kDecodeBlockKeys = 64;
+
+// Prefill: the three tensor maps describe q, k, v as 3-D [B*H][N][d] bf16 tensors with
+// 64-element (128-byte) inner boxes of 128 rows and 128-byte swizzle.
+cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
+                           cudaStream_t stream);
+
+cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+
+}  // namespace fattn

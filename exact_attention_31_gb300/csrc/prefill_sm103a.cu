@@ -1,0 +1,477 @@
+// prefill_sm103a.cu -- fused exact attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes is the FlashAttention-2 forward loop nest ("Flash Attention: The Hidden Gem",
+// The Algorithm, steps 3-7): for each query tile, carry a running max m, a running sum l and an
+// unnormalised output O per row; for each key/value tile compute S = Q K^T, raise m, rescale l and
+// O by exp(m_old - m_new) (The Correction Factor), add P = exp(S - m) and P V; after the last tile
+// write O / l and L = m + log(l).  S and P live only in tensor memory.
+//
+// How it maps onto one SM (one CTA per SM, 320 threads):
+//   warps 0-3  softmax group for query tile 0 (one thread per query row / TMEM lane)
+//   warps 4-7  softmax group for query tile 1
+//   warp  8    TMA producer: Q tiles once, then K_j, V_j through a ring of shared-memory slots
+//   warp  9    MMA issuer (one thread) and TMEM owner
+// Tensor memory (512 columns x 128 lanes, fp32): S_t at columns 128t, O_t at 256 + 128t; the bf16
+// probabilities P_t are written over the first 64 columns of S_t and fed to the second MMA
+// straight from TMEM.  Two query tiles per CTA let the tensor core work on one tile's S or P V
+// while the other tile's softmax runs.
+//
+// Scores are handled in log2 units: with c = scale * log2(e), exp(scale * s - scale * m) is
+// exp2(s * c - m * c), one FFMA and one ex2 per element.  The running max used as the exponent
+// reference is only raised when the tile max exceeds it by more than kRescaleLog2 (the rescale is
+// exact for any reference as long as l, O and L use the same one: exp(a-c) = exp(a-b) exp(b-c),
+// "FlashAttention: attention was never compute-bound", On the maths anxiety), which keeps most
+// tiles from touching O in TMEM at all.  Two row sums are kept: l from the fp32 weights, which
+// gives L = m + log(l), and lr from the bf16-rounded weights that enter P V, which normalises O so
+// that its numerator and denominator see the same weights.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fattn_internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace fattn {
+namespace {
+
+constexpr int kBlockM = 128;       // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;       // keys per key/value tile
+constexpr int kTiles = 2;          // query tiles per CTA
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAtomBytes = kBlockM * 128;  // one 128-row x 128-byte swizzled chunk
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr uint32_t kTileBytes = kBlockM * D * 2;
+  static constexpr int kSlots = (D == 64) ? 6 : 4;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKVOff = kQOff + kTiles * kTileBytes;
+  static constexpr uint32_t kBarOff = kKVOff + kSlots * kTileBytes;
+  // barrier indices
+  static constexpr int kQFull = 0;             // [2]
+  static constexpr int kSFull = 2;             // [2]
+  static constexpr int kPFull = 4;             // [2]
+  static constexpr int kOFull = 6;             // [2]
+  static constexpr int kDrain = 8;             // [1]
+  static constexpr int kKVFull = 9;            // [kSlots]
+  static constexpr int kKVEmpty = 9 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 9 + 2 * kSlots;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+};
+
+struct Args {
+  __nv_bfloat16* o;
+  float* lse;
+  int BH, Nq, Nk, causal;
+  int units_per_head;  // ceil(Nq / 256)
+  float c_log2;        // scale * log2(e)
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+// Number of key/value tiles query tile [r0, r0 + 128) must visit (0 if the tile is past Nq).
+__device__ __forceinline__ int tiles_needed(int r0, const Args& a) {
+  if (r0 >= a.Nq) return 0;
+  int last_key = a.Nk - 1;
+  if (a.causal) last_key = min(last_key, r0 + kBlockM - 1 + (a.Nk - a.Nq));
+  return last_key / kBlockN + 1;
+}
+
+__device__ __forceinline__ void wait_dep(uint32_t (&r)[32]) {
+  // tcgen05.wait::ld that also ties the loaded registers, so no use can be scheduled above it
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+        "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+        "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+struct Abort {
+  volatile uint32_t* flag;
+  unsigned int* status;
+  uint64_t deadline;
+  __device__ void raise() const {
+    *flag = 1u;
+    atomicOr(status, kStatusTimeout);
+  }
+};
+
+// Every thread of a warp waits; the outcome is made warp-uniform so the warp stays converged for
+// the .sync.aligned tensor-memory instructions that follow.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  bool ok = mbar_wait_bounded(bar, parity, ab.flag, ab.deadline);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) ab.raise();
+  return ok;
+}
+
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  const bool ok = mbar_wait_bounded(bar, parity, ab.flag, ab.deadline);
+  if (!ok) ab.raise();
+  return ok;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Softmax group: one thread per query row.
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int bh, uint32_t tmem,
+                                             uint32_t sbar, const Args& a, const Abort& ab) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int q_row = row0 + t * kBlockM + quarter * 32 + lane;
+  const int limit = a.causal ? min(q_row + (a.Nk - a.Nq), a.Nk - 1) : a.Nk - 1;
+  const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t tS = tmem + lane_field + static_cast<uint32_t>(t * 128);
+  const uint32_t tO = tmem + lane_field + static_cast<uint32_t>(256 + t * 128);
+  const float c = a.c_log2;
+
+  float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
+  float l = 0.f;   // sum of the fp32 weights: L = m + log(l)
+  float lr = 0.f;  // sum of the bf16-rounded weights that entered P V: O = O / lr
+  bool ok = true;
+  for (int j = 0; j < n_tiles; ++j) {
+    if (!warp_wait(sbar + 8 * (C::kSFull + t), j & 1, ab)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t s[4][32];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x32(tS + 32 * h, s[h]);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) wait_dep(s[h]);
+
+    const int kv0 = j * kBlockN;
+    if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > limit)) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (kv0 + 32 * h + i > limit) s[h][i] = __float_as_uint(-INFINITY);
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[h][i]));
+    const float m_new = fmaxf(m_ref, mx * c);
+    const bool need = m_new > m_ref + kRescaleLog2;
+    float corr = 1.f;
+    if (need) {
+      corr = ex2_approx(m_ref - m_new);  // 0 on the first tile
+      m_ref = m_new;
+      l *= corr;
+      lr *= corr;
+    }
+    const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+    uint32_t p[2][32];
+    float lsum = 0.f, lrsum = 0.f;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float e0 = ex2_approx(fmaf(__uint_as_float(s[h][2 * i]), c, neg_m));
+        const float e1 = ex2_approx(fmaf(__uint_as_float(s[h][2 * i + 1]), c, neg_m));
+        const uint32_t pk = pack_bf16x2(e0, e1);
+        p[h >> 1][(h & 1) * 16 + i] = pk;
+        lsum += e0 + e1;
+        lrsum += bf16lo_to_f32(pk) + bf16hi_to_f32(pk);
+      }
+    }
+    l += lsum;
+    lr += lrsum;
+    tmem_st_32x32b_x32(tS, p[0]);
+    tmem_st_32x32b_x32(tS + 32, p[1]);
+
+    // O_t was last written by P V of tile j-1, which completed before S_t(j) did.
+    if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int h = 0; h < D / 32; ++h) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tO + 32 * h, o);
+        wait_dep(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+        tmem_st_32x32b_x32(tO + 32 * h, o);
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(sbar + 8 * (C::kPFull + t));
+  }
+  if (!ok || n_tiles == 0) return;
+
+  if (!warp_wait(sbar + 8 * (C::kOFull + t), 0, ab)) return;
+  tc_fence_after();
+  const float inv_l = 1.f / lr;
+  const bool store = q_row < a.Nq;
+  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
+#pragma unroll
+  for (int h = 0; h < D / 32; ++h) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + 32 * h, o);
+    wait_dep(o);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + 32 * h);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+  if (store && a.lse != nullptr) {
+    a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// TMA producer (one thread)
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk,
+                                              const CUtensorMap* tv, const int (&n)[2], int row0,
+                                              int bh, uint32_t sbase, const Abort& ab) {
+  using C = Cfg<D>;
+  const uint32_t sbar = sbase + C::kBarOff;
+  tma_prefetch_desc(tq);
+  tma_prefetch_desc(tk);
+  tma_prefetch_desc(tv);
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    if (n[t] == 0) continue;
+    const uint32_t bar = sbar + 8 * (C::kQFull + t);
+    mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+    for (int ch = 0; ch < C::kChunks; ++ch)
+      tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + ch * kAtomBytes, tq, bar, ch * 64,
+                  row0 + t * kBlockM, bh);
+  }
+  const int nmax = max(n[0], n[1]);
+  int issued = 0;
+  bool ok = true;
+  for (int j = 0; j < nmax && ok; ++j) {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int idx = 2 * j + w;
+      const int slot = idx % C::kSlots;
+      const int round = idx / C::kSlots;
+      if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) {
+        ok = false;
+        break;
+      }
+      const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
+      mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+      for (int ch = 0; ch < C::kChunks; ++ch)
+        tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + ch * kAtomBytes, w ? tv : tk, bar,
+                    ch * 64, j * kBlockN, bh);
+      ++issued;
+    }
+  }
+  if (!ok) {
+    // Let the copies already in flight land before the CTA's shared memory goes away.
+    const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
+    volatile uint32_t never = 0;
+    for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx) {
+      const int slot = idx % C::kSlots;
+      mbar_wait_bounded(sbar + 8 * (C::kKVFull + slot), (idx / C::kSlots) & 1, &never, until);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void mma_role(const int (&n)[2], uint32_t tmem, uint32_t sbase,
+                                         const Abort& ab) {
+  using C = Cfg<D>;
+  const uint32_t sbar = sbase + C::kBarOff;
+  constexpr uint32_t kIdS = mma_idesc_bf16_f32(kBlockM, kBlockN, false);
+  constexpr uint32_t kIdPV = mma_idesc_bf16_f32(kBlockM, D, true);
+  bool ok = true;
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t)
+    if (n[t] > 0 && ok) ok = thread_wait(sbar + 8 * (C::kQFull + t), 0, ab);
+  const int nmax = max(n[0], n[1]);
+  for (int j = 0; j <= nmax && ok; ++j) {
+    int kslot = 0, vslot = 0;
+    if (j < nmax) {
+      const int idx = 2 * j;
+      kslot = idx % C::kSlots;
+      if (!thread_wait(sbar + 8 * (C::kKVFull + kslot), (idx / C::kSlots) & 1, ab)) {
+        ok = false;
+        break;
+      }
+    }
+    if (j > 0) {
+      const int idx = 2 * (j - 1) + 1;
+      vslot = idx % C::kSlots;
+      if (!thread_wait(sbar + 8 * (C::kKVFull + vslot), (idx / C::kSlots) & 1, ab)) {
+        ok = false;
+        break;
+      }
+    }
+    tc_fence_after();
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+      if (j > 0 && j - 1 < n[t]) {
+        // O_t += P_t(j-1) V_{j-1}: A from TMEM (bf16 pairs packed per column), B = V MN-major.
+        if (!thread_wait(sbar + 8 * (C::kPFull + t), (j - 1) & 1, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = sbase + C::kKVOff + vslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, kAtomBytes, 1024);
+          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, bdesc, kIdPV,
+                 (j - 1 > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (j - 1 == n[t] - 1) mma_commit(sbar + 8 * (C::kOFull + t));
+      }
+      if (j < n[t]) {
+        // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzled, 16 keys of d per step.
+        const uint32_t q_addr = sbase + C::kQOff + t * C::kTileBytes;
+        const uint32_t k_addr = sbase + C::kKVOff + kslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          mma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
+                 smem_desc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(sbar + 8 * (C::kSFull + t));
+      }
+    }
+    if (!ok) break;
+    if (j < nmax) mma_commit(sbar + 8 * (C::kKVEmpty + kslot));
+    if (j > 0) mma_commit(sbar + 8 * (C::kKVEmpty + vslot));
+  }
+  if (!ok) {
+    // Make sure no MMA is still writing tensor memory when it is freed.
+    mma_commit(sbar + 8 * C::kDrain);
+    volatile uint32_t never = 0;
+    mbar_wait_bounded(sbar + 8 * C::kDrain, 0, &never, globaltimer_ns() + 50ull * 1000 * 1000);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const Args a) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const uint32_t sbar = sbase + C::kBarOff;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+
+  // Heaviest causal work first: the last query blocks of every head are launched first.
+  const int unit = a.units_per_head - 1 - static_cast<int>(blockIdx.x) / a.BH;
+  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int row0 = unit * kTiles * kBlockM;
+  int n[2];
+  n[0] = tiles_needed(row0, a);
+  n[1] = tiles_needed(row0 + kBlockM, a);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(sbar + 8 * (C::kQFull + t), 1);
+      mbar_init(sbar + 8 * (C::kSFull + t), 1);
+      mbar_init(sbar + 8 * (C::kPFull + t), kBlockM);
+      mbar_init(sbar + 8 * (C::kOFull + t), 1);
+    }
+    mbar_init(sbar + 8 * C::kDrain, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(sbar + 8 * (C::kKVFull + s), 1);
+      mbar_init(sbar + 8 * (C::kKVEmpty + s), 1);
+    }
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  Abort ab{abort_flag, a.status, globaltimer_ns() + a.timeout_ns};
+
+  if (warp < 8) {
+    const int t = warp >> 2;
+    softmax_role<D>(t, n[t], row0, bh, tmem, sbar, a, ab);
+  } else if (warp == kProducerWarp) {
+    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, n, row0, bh, sbase, ab);
+    __syncwarp();
+  } else {
+    if ((threadIdx.x & 31) == 0) mma_role<D>(n, tmem, sbase, ab);
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
+                     cudaStream_t stream) {
+  using C = Cfg<D>;
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  Args a;
+  a.o = static_cast<__nv_bfloat16*>(p.o);
+  a.lse = p.lse;
+  a.BH = p.B * p.H;
+  a.Nq = p.Nq;
+  a.Nk = p.Nk;
+  a.causal = p.causal;
+  a.units_per_head = (p.Nq + kTiles * kBlockM - 1) / (kTiles * kBlockM);
+  a.c_log2 = p.scale * 1.4426950408889634f;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  const unsigned int grid = static_cast<unsigned int>(a.units_per_head) * static_cast<unsigned int>(a.BH);
+  prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
+                           cudaStream_t stream) {
+  if (p.d == 64) return launch_d<64>(p, tq, tk, tv, status, timeout_ns, stream);
+  return launch_d<128>(p, tq, tk, tv, status, timeout_ns, stream);
+}
+
+}  // namespace fattn

@@ -1,0 +1,120 @@
+/*
+ * fattn.h -- C ABI of libfattn: exact fused attention forward and split-KV decode for sm_103a.
+ *
+ * The operation is the one the pages define: O = softmax(scale * Q K^T + mask) V, computed tile by
+ * tile with the online-softmax recurrence (running max m, running sum l, unnormalised O rescaled by
+ * exp(m_old - m_new)), so that the N x N score and probability matrices never reach device memory,
+ * and L = m + log(l) emitted per query row.
+ *   - "Flash Attention: The Hidden Gem", sections Background, Online Softmax, The Algorithm
+ *     (steps 3-7) and The Correction Factor.
+ *   - "FlashAttention: attention was never compute-bound", section The one formula.
+ *   - "Understanding FlashAttention", section Attention: Q and the output are [N, D], K and V are
+ *     [M, D]; decoding one token is N = 1 against M cached keys; batch and heads only repeat
+ *     independent problems.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors live in device memory, are contiguous and row-major, and are owned by the caller.
+ *     The library allocates no device memory in any call and keeps no pointer after a call returns.
+ *   - bf16 means IEEE-style bfloat16 (1-8-7), stored as 16-bit words.  Accumulation is fp32.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.  Calls are
+ *     asynchronous and stream-ordered: they return after enqueueing work.
+ *   - Every argument is checked on the host before anything is launched.  A rejected call returns
+ *     FATTN_ERR_INVALID_ARG or FATTN_ERR_UNSUPPORTED and launches nothing.
+ *   - Device pointers must be 16-byte aligned.
+ *   - A returned FATTN_ERR_CUDA means a launch was refused by the CUDA runtime; the runtime's own
+ *     error state is left for the caller to read.
+ */
+#ifndef FATTN_H_
+#define FATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fattn_status {
+  FATTN_OK = 0,
+  FATTN_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, a non-positive size, a bad scale ... */
+  FATTN_ERR_UNSUPPORTED = 2, /* a head dimension other than 64 or 128 */
+  FATTN_ERR_CUDA = 3,        /* the CUDA runtime refused a launch or an attribute call */
+  FATTN_ERR_TIMEOUT = 4      /* a bounded on-device wait gave up (see fattn_last_error) */
+} fattn_status;
+
+/*
+ * fattn_fwd -- fused attention forward ("Flash Attention: The Hidden Gem", The Algorithm).
+ *
+ *   q    bf16 [B, H, Nq, d]      queries
+ *   k    bf16 [B, H, Nk, d]      keys
+ *   v    bf16 [B, H, Nk, d]      values
+ *   o    bf16 [B, H, Nq, d]      output, written: O_i = diag(l_i)^-1 * O_i (step 6)
+ *   lse  fp32 [B, H, Nq] or NULL log-sum-exp per row, natural log of sum_j exp(scale * q_i.k_j)
+ *                                over the visible keys, i.e. L = m + log(l) (step 6)
+ *   B, H, Nq, Nk >= 1; d in {64, 128}
+ *   causal  0 or 1.  With 1, query row i sees key j iff j <= i + (Nk - Nq) (bottom-right
+ *           alignment; the usual lower triangle when Nq == Nk).  Requires Nq <= Nk, so that every
+ *           row sees at least one key.
+ *   scale   finite and > 0 (typically 1/sqrt(d)).
+ *
+ * The kernel reads Q, K and V and writes O and L; no score or probability tile leaves the chip.
+ */
+fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                       int Nq, int Nk, int d, int causal, float scale, void* stream);
+
+/*
+ * fattn_decode_num_splits -- the number of key splits fattn_decode uses for a request.
+ *
+ * The cached keys are cut into blocks of 64; nblk = ceil(Nk / 64).  `num_splits` = 0 asks for the
+ * default, one partial state per 64-key block (nblk splits).  A value in [1, nblk] is used as given;
+ * split s then covers blocks [s*nblk/S, (s+1)*nblk/S).  Returns the resolved count, or -1 if the
+ * request is invalid (Nk < 1 or num_splits outside [0, nblk]).
+ */
+int fattn_decode_num_splits(int Nk, int num_splits);
+
+/*
+ * fattn_decode_workspace_size -- bytes of scratch fattn_decode needs for these sizes.
+ *
+ * The workspace holds one partial state (m, l, unnormalised O[d]) in fp32 per (b, h, split).
+ * Returns 0 if the sizes are invalid.
+ */
+size_t fattn_decode_workspace_size(int B, int H, int Nk, int d, int num_splits);
+
+/*
+ * fattn_decode -- one query token per (b, h) against a KV cache (Nq = 1; "Understanding
+ * FlashAttention", Attention: "when decoding one token, N = 1").  No mask: every cached key is
+ * visible.
+ *
+ *   q        bf16 [B, H, 1, d]
+ *   k_cache  bf16 [B, H, Nk, d]
+ *   v_cache  bf16 [B, H, Nk, d]
+ *   o        bf16 [B, H, 1, d]       output
+ *   lse      fp32 [B, H, 1] or NULL  natural-log log-sum-exp of the scaled scores
+ *   workspace  device scratch of at least fattn_decode_workspace_size(B, H, Nk, d, num_splits)
+ *              bytes, 16-byte aligned, owned by the caller; its contents on entry do not matter and
+ *              on return are unspecified.  Two calls in flight at once must not share it.
+ *
+ * Two kernels run on `stream`: a split kernel that streams each split's keys and values once and
+ * leaves a partial (m, l, O) per split, and a combine kernel that merges the partials with the
+ * correction-factor rule (m = max m_s, l = sum exp(m_s - m) l_s, O = sum exp(m_s - m) O_s / l;
+ * "Flash Attention: The Hidden Gem", The Correction Factor) and writes O and L.
+ */
+fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                          int B, int H, int Nk, int d, float scale, int num_splits, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * fattn_last_error -- wait for `stream`, then read and clear the library's on-device status word on
+ * the current device.  Returns FATTN_OK, FATTN_ERR_TIMEOUT if some kernel's bounded wait gave up
+ * since the last read (its outputs are then unspecified), or FATTN_ERR_CUDA if the stream reported
+ * an error.
+ */
+fattn_status fattn_last_error(void* stream);
+
+/* fattn_status_string -- a static, human-readable name for a status code (never NULL). */
+const char* fattn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H_ */

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol, and rejects bad
+arguments before touching the GPU (these calls return before any CUDA call, so they run anywhere).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from exact_attention_31_gb300 import _build
+    _build.build()
+    import exact_attention_31_gb300 as fa
+    return fa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fattn_fwd", "fattn_decode", "fattn_decode_workspace_size", "fattn_status_string",
+                     "fattn_last_error", "fattn_decode_num_splits"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libfattn.so does not export {name}"
+
+
+def test_status_strings(L):
+    import exact_attention_31_gb300 as fa
+    assert fa.fattn_status_string(0) == "FATTN_OK"
+    assert fa.fattn_status_string(4) == "FATTN_ERR_TIMEOUT"
+    assert fa.fattn_status_string(99) == "FATTN_UNKNOWN_STATUS"
+
+
+A = 4096  # a 16-byte-aligned fake address: never dereferenced, the checks reject the call first
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, A, A, A, None, 1, 1, 8, 8, 64, 0, 0.125), 1),       # null q
+    ((A, A, A, A + 2, None, 1, 1, 8, 8, 64, 0, 0.125), 1),      # misaligned o
+    ((A, A, A, A, A + 1, 1, 1, 8, 8, 64, 0, 0.125), 1),         # misaligned lse
+    ((A, A, A, A, None, 0, 1, 8, 8, 64, 0, 0.125), 1),          # B = 0
+    ((A, A, A, A, None, 1, 1, 0, 8, 64, 0, 0.125), 1),          # Nq = 0
+    ((A, A, A, A, None, 1, 1, 9, 8, 64, 1, 0.125), 1),          # causal with Nq > Nk
+    ((A, A, A, A, None, 1, 1, 8, 8, 64, 2, 0.125), 1),          # causal flag not 0/1
+    ((A, A, A, A, None, 1, 1, 8, 8, 64, 0, 0.0), 1),            # scale 0
+    ((A, A, A, A, None, 1, 1, 8, 8, 64, 0, float("nan")), 1),   # scale NaN
+    ((A, A, A, A, None, 1, 1, 8, 8, 64, 0, float("inf")), 1),   # scale inf
+    ((A, A, A, A, None, 1, 1, 8, 8, 96, 0, 0.125), 2),          # d unsupported
+    ((A, A, A, A, None, 1, 1, 8, 8, 32, 0, 0.125), 2),
+])
+def test_fwd_rejects_bad_arguments(L, args, expect):
+    assert L.fattn_fwd(*args, None) == expect
+
+
+def test_decode_split_resolution(L):
+    assert L.fattn_decode_num_splits(16384, 0) == 256
+    assert L.fattn_decode_num_splits(65, 0) == 2
+    assert L.fattn_decode_num_splits(1, 0) == 1
+    assert L.fattn_decode_num_splits(1000, 16) == 16
+    assert L.fattn_decode_num_splits(1000, 17) == -1
+    assert L.fattn_decode_num_splits(0, 0) == -1
+    assert L.fattn_decode_num_splits(100, -1) == -1
+
+
+def test_decode_workspace_size(L):
+    # one fp32 (m, l, O[d]) per (b, h, split), each array padded to 256 bytes
+    def pad(x):
+        return (x + 255) // 256 * 256
+    assert L.fattn_decode_workspace_size(32, 32, 16384, 128, 0) == pad(32 * 32 * 256 * 128 * 4) + pad(32 * 32 * 256 * 2 * 4)
+    assert L.fattn_decode_workspace_size(1, 1, 1, 64, 0) == 256 + 256
+    assert L.fattn_decode_workspace_size(0, 1, 1, 64, 0) == 0
+    assert L.fattn_decode_workspace_size(1, 1, 100, 64, 3) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, A, A, A, None, 1, 1, 64, 64, 0.125, 0, A, 1 << 20), 1),
+    ((A, A, A, A, None, 1, 1, 64, 64, 0.125, 0, None, 1 << 20), 1),     # no workspace
+    ((A, A, A, A, None, 1, 1, 64, 64, 0.125, 0, A, 16), 1),             # workspace too small
+    ((A, A, A, A, None, 1, 1, 64, 64, 0.125, 0, A + 8, 1 << 20), 1),    # misaligned workspace
+    ((A, A, A, A, None, 1, 1, 0, 64, 0.125, 0, A, 1 << 20), 1),         # Nk = 0
+    ((A, A, A, A, None, 1, 1, 64, 64, 0.125, 2, A, 1 << 20), 1),        # more splits than blocks
+    ((A, A, A, A, None, 1, 1, 64, 64, -1.0, 0, A, 1 << 20), 1),         # negative scale
+    ((A, A, A, A, None, 1, 1, 64, 80, 0.125, 0, A, 1 << 20), 2),        # d unsupported
+])
+def test_decode_rejects_bad_arguments(L, args, expect):
+    assert L.fattn_decode(*args, None) == expect
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    import exact_attention_31_gb300 as fa
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fattn_fwd(q, q, q)
