@@ -101,7 +101,7 @@ def recorded_traffic(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms in the background; samples carry host timestamps."""
+    """nvidia-smi sampled every 50 ms in the background; samples carry host timestamps."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -117,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -572,8 +572,8 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description="exact-attention hot-path benchmark")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
                     help="both = the benchmark step; the others time one half (used for profiling)")

@@ -11,10 +11,13 @@
 //   warps 4-7  softmax group for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_j, V_j through a ring of shared-memory slots
 //   warp  9    MMA issuer (one thread) and TMEM owner
-// Tensor memory (512 columns x 128 lanes, fp32): S_t at columns 128t, O_t at 256 + 128t; the bf16
-// probabilities P_t are written over the first 64 columns of S_t and fed to the second MMA
-// straight from TMEM.  Two query tiles per CTA let the tensor core work on one tile's S or P V
-// while the other tile's softmax runs.
+// Tensor memory (512 columns x 128 lanes, fp32): S_t at columns 128t and O_t at 256 + 128t.  The
+// bf16 probabilities P_t are fed to the second MMA straight from TMEM.  With d = 64, O_t uses only
+// half of its 128 columns and P_t gets the other half, so S_t(j+1) = Q_t K_{j+1}^T can be issued
+// as soon as the softmax group has read S_t(j) into registers: the tensor core computes the next
+// scores while the current ones are exponentiated.  With d = 128 tensor memory is full and P_t is
+// written over the first 64 columns of S_t, so S_t(j+1) follows P_t(j) V_j.  Two query tiles per
+// CTA let the tensor core work on one tile while the other tile's softmax runs.
 //
 // Scores are handled in log2 units: with c = scale * log2(e), exp(scale * s - scale * m) is
 // exp2(s * c - m * c), one FFMA and one ex2 per element.  The running max used as the exponent
@@ -23,7 +26,9 @@
 // "FlashAttention: attention was never compute-bound", On the maths anxiety), which keeps most
 // tiles from touching O in TMEM at all.  Two row sums are kept: l from the fp32 weights, which
 // gives L = m + log(l), and lr from the bf16-rounded weights that enter P V, which normalises O so
-// that its numerator and denominator see the same weights.
+// that its numerator and denominator see the same weights.  The per-row arithmetic uses packed
+// fp32x2 FMA/add and three-input max with several independent accumulators, so one thread's row
+// is not a single long dependency chain.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -45,6 +50,7 @@ constexpr uint32_t kAtomBytes = kBlockM * 128;  // one 128-row x 128-byte swizzl
 
 template <int D>
 struct Cfg {
+  static constexpr bool kSepP = (D == 64);  // P_t has TMEM columns of its own (see above)
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kTileBytes = kBlockM * D * 2;
   static constexpr int kSlots = (D == 64) ? 6 : 4;
@@ -52,16 +58,22 @@ struct Cfg {
   static constexpr uint32_t kKVOff = kQOff + kTiles * kTileBytes;
   static constexpr uint32_t kBarOff = kKVOff + kSlots * kTileBytes;
   // barrier indices
-  static constexpr int kQFull = 0;             // [2]
-  static constexpr int kSFull = 2;             // [2]
-  static constexpr int kPFull = 4;             // [2]
-  static constexpr int kOFull = 6;             // [2]
-  static constexpr int kDrain = 8;             // [1]
-  static constexpr int kKVFull = 9;            // [kSlots]
-  static constexpr int kKVEmpty = 9 + kSlots;  // [kSlots]
-  static constexpr int kNumBars = 9 + 2 * kSlots;
+  static constexpr int kQFull = 0;              // [2] Q_t landed
+  static constexpr int kSFull = 2;              // [2] S_t computed
+  static constexpr int kSFree = 4;              // [2] S_t read into registers (separate-P only)
+  static constexpr int kPFull = 6;              // [2] P_t written, O_t corrected
+  static constexpr int kPVDone = 8;             // [2] O_t += P_t V done (separate-P only)
+  static constexpr int kOFull = 10;             // [2] last P V of tile t done
+  static constexpr int kDrain = 12;             // [1] wind-down after a timeout
+  static constexpr int kKVFull = 13;            // [kSlots]
+  static constexpr int kKVEmpty = 13 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 13 + 2 * kSlots;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  // tensor-memory columns
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
+  __host__ __device__ static constexpr uint32_t col_p(int t) { return kSepP ? 256u + 128u * t + 64u : 128u * t; }
 };
 
 struct Args {
@@ -119,6 +131,41 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const
 }
 
 // ------------------------------------------------------------------------------------------------
+// Packed fp32 helpers (sm_100+): two lanes of fp32 per instruction.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (o0, o1) = (a0, a1) * b + c
+__device__ __forceinline__ void ffma2_bc(float& o0, float& o1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %5};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(o0), "=f"(o1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (a0, a1) += (b0, b1)
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// a0 += low bf16 of pk, a1 += high bf16 of pk (mixed-precision adds, exact widening)
+__device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(pk));
+}
+
+// ------------------------------------------------------------------------------------------------
 // Softmax group: one thread per query row.
 // ------------------------------------------------------------------------------------------------
 template <int D>
@@ -130,13 +177,14 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
   const int q_row = row0 + t * kBlockM + quarter * 32 + lane;
   const int limit = a.causal ? min(q_row + (a.Nk - a.Nq), a.Nk - 1) : a.Nk - 1;
   const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t tS = tmem + lane_field + static_cast<uint32_t>(t * 128);
-  const uint32_t tO = tmem + lane_field + static_cast<uint32_t>(256 + t * 128);
+  const uint32_t tS = tmem + lane_field + C::col_s(t);
+  const uint32_t tO = tmem + lane_field + C::col_o(t);
+  const uint32_t tP = tmem + lane_field + C::col_p(t);
   const float c = a.c_log2;
 
   float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
-  float l = 0.f;   // sum of the fp32 weights: L = m + log(l)
-  float lr = 0.f;  // sum of the bf16-rounded weights that entered P V: O = O / lr
+  float l = 0.f;            // sum of the fp32 weights: L = m + log(l)
+  float lr = 0.f;           // sum of the bf16-rounded weights that entered P V: O = O / lr
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
     if (!warp_wait(sbar + 8 * (C::kSFull + t), j & 1, ab)) {
@@ -149,6 +197,12 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
     for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x32(tS + 32 * h, s[h]);
 #pragma unroll
     for (int h = 0; h < 4; ++h) wait_dep(s[h]);
+    if constexpr (C::kSepP) {
+      // S_t is in registers: the MMA warp may compute the next S_t into the same columns.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbar + 8 * (C::kSFree + t));
+    }
 
     const int kv0 = j * kBlockN;
     if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > limit)) {
@@ -158,11 +212,19 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
         for (int i = 0; i < 32; ++i)
           if (kv0 + 32 * h + i > limit) s[h][i] = __float_as_uint(-INFINITY);
     }
-    float mx = -INFINITY;
+    // row max: eight independent three-input chains
+    float mx8[8];
 #pragma unroll
-    for (int h = 0; h < 4; ++h)
+    for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[0][2 * k]), __uint_as_float(s[0][2 * k + 1]));
 #pragma unroll
-      for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[h][i]));
+    for (int e = 16; e < 128; e += 16) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mx8[k] = max3f(mx8[k], __uint_as_float(s[(e + 2 * k) >> 5][(e + 2 * k) & 31]),
+                       __uint_as_float(s[(e + 2 * k + 1) >> 5][(e + 2 * k + 1) & 31]));
+    }
+    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), fmaxf(max3f(mx8[3], mx8[4], mx8[5]),
+                                                                max3f(mx8[6], mx8[7], mx8[7])));
     const float m_new = fmaxf(m_ref, mx * c);
     const bool need = m_new > m_ref + kRescaleLog2;
     float corr = 1.f;
@@ -175,25 +237,40 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
     const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
     uint32_t p[2][32];
-    float lsum = 0.f, lrsum = 0.f;
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of fp32 partial sums
+    float lrs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float e0 = ex2_approx(fmaf(__uint_as_float(s[h][2 * i]), c, neg_m));
-        const float e1 = ex2_approx(fmaf(__uint_as_float(s[h][2 * i + 1]), c, neg_m));
+        float x0, x1;
+        ffma2_bc(x0, x1, __uint_as_float(s[h][2 * i]), __uint_as_float(s[h][2 * i + 1]), c, neg_m);
+        const float e0 = ex2_approx(x0);
+        const float e1 = ex2_approx(x1);
         const uint32_t pk = pack_bf16x2(e0, e1);
         p[h >> 1][(h & 1) * 16 + i] = pk;
-        lsum += e0 + e1;
-        lrsum += bf16lo_to_f32(pk) + bf16hi_to_f32(pk);
+        const int acc = (i & 1) * 2;
+        fadd2(ls[acc], ls[acc + 1], e0, e1);
+        add_bf16x2(lrs[acc], lrs[acc + 1], pk);
       }
     }
-    l += lsum;
-    lr += lrsum;
-    tmem_st_32x32b_x32(tS, p[0]);
-    tmem_st_32x32b_x32(tS + 32, p[1]);
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    lr += (lrs[0] + lrs[1]) + (lrs[2] + lrs[3]);
 
-    // O_t was last written by P V of tile j-1, which completed before S_t(j) did.
+    if constexpr (C::kSepP) {
+      // P_t and O_t are still read by P_t(j-1) V_{j-1} until it completes.
+      if (j > 0) {
+        if (!warp_wait(sbar + 8 * (C::kPVDone + t), (j - 1) & 1, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+    }
+    tmem_st_32x32b_x32(tP, p[0]);
+    tmem_st_32x32b_x32(tP + 32, p[1]);
+
+    // Rescale O_t (last written by P_t(j-1) V_{j-1}, now complete) when the reference moved.
     if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int h = 0; h < D / 32; ++h) {
@@ -201,13 +278,19 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
         tmem_ld_32x32b_x32(tO + 32 * h, o);
         wait_dep(o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+        for (int i = 0; i < 32; i += 2) {
+          float y0, y1;
+          ffma2_bc(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), corr, 0.f);
+          o[i] = __float_as_uint(y0);
+          o[i + 1] = __float_as_uint(y1);
+        }
         tmem_st_32x32b_x32(tO + 32 * h, o);
       }
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(sbar + 8 * (C::kPFull + t));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sbar + 8 * (C::kPFull + t));
   }
   if (!ok || n_tiles == 0) return;
 
@@ -292,80 +375,155 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
 }
 
 // ------------------------------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuer: the whole warp runs the schedule (its waits and indices are warp-uniform) and one
+// elected lane issues the tcgen05 instructions.  Every shared-memory descriptor is built once; a
+// step of K only adds a constant to the start-address field, so issuing an MMA is one 64-bit add.
 // ------------------------------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void mma_role(const int (&n)[2], uint32_t tmem, uint32_t sbase,
-                                         const Abort& ab) {
+struct MmaCtx {
   using C = Cfg<D>;
-  const uint32_t sbar = sbase + C::kBarOff;
-  constexpr uint32_t kIdS = mma_idesc_bf16_f32(kBlockM, kBlockN, false);
-  constexpr uint32_t kIdPV = mma_idesc_bf16_f32(kBlockM, D, true);
-  bool ok = true;
+  uint32_t tmem, sbar;
+  uint64_t dq[kTiles];  // Q_t, K-major
+  uint64_t dk0;         // slot 0 as a K-major operand (K_j)
+  uint64_t dv0;         // slot 0 as an MN-major operand (V_j)
+  uint32_t lead;  // non-zero in the one lane that issues
+
+  __device__ __forceinline__ void init(uint32_t tmem_, uint32_t sbase) {
+    tmem = tmem_;
+    sbar = sbase + C::kBarOff;
 #pragma unroll
-  for (int t = 0; t < kTiles; ++t)
-    if (n[t] > 0 && ok) ok = thread_wait(sbar + 8 * (C::kQFull + t), 0, ab);
+    for (int t = 0; t < kTiles; ++t) dq[t] = smem_desc_sw128(sbase + C::kQOff + t * C::kTileBytes, 16, 1024);
+    dk0 = smem_desc_sw128(sbase + C::kKVOff, 16, 1024);
+    dv0 = smem_desc_sw128(sbase + C::kKVOff, kAtomBytes, 1024);
+    lead = elect_lane();
+  }
+  // start-address field advance (16-byte units)
+  __host__ __device__ static constexpr uint64_t slot_adv(int slot) { return static_cast<uint64_t>(slot) * (C::kTileBytes >> 4); }
+  __host__ __device__ static constexpr uint64_t kmajor_adv(int kk) { return static_cast<uint64_t>((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4; }
+  __host__ __device__ static constexpr uint64_t vstep_adv(int kk) { return static_cast<uint64_t>(kk * 16 * 128) >> 4; }
+
+  // S_t = Q_t K^T: both operands K-major, 16 elements of d per instruction.
+  __device__ __forceinline__ void issue_s(int t, int kslot) const {
+    constexpr uint32_t kIdS = mma_idesc_bf16_f32(kBlockM, kBlockN, false);
+    const uint64_t a = dq[t], b = dk0 + slot_adv(kslot);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ss_lead(tmem + C::col_s(t), a + kmajor_adv(kk), b + kmajor_adv(kk), kIdS, kk > 0 ? 1u : 0u, lead);
+  }
+  // O_t += P_t V: A from TMEM (bf16 pairs packed per column), B = V MN-major, 16 keys per step.
+  __device__ __forceinline__ void issue_pv(int t, int vslot, bool first) const {
+    constexpr uint32_t kIdPV = mma_idesc_bf16_f32(kBlockM, D, true);
+    const uint64_t b = dv0 + slot_adv(vslot);
+#pragma unroll
+    for (int kk = 0; kk < kBlockN / 16; ++kk)
+      mma_ts_lead(tmem + C::col_o(t), tmem + C::col_p(t) + 8 * kk, b + vstep_adv(kk), kIdPV,
+                  (!first || kk > 0) ? 1u : 0u, lead);
+  }
+  __device__ __forceinline__ void commit(int bar) const { mma_commit_lead(sbar + 8 * bar, lead); }
+  // KV ring index of K_j is 2j, of V_j is 2j + 1.
+  __device__ __forceinline__ bool wait_kv(int idx, const Abort& ab) const {
+    return warp_wait(sbar + 8 * (C::kKVFull + idx % C::kSlots), (idx / C::kSlots) & 1, ab);
+  }
+  __device__ __forceinline__ bool wait(int bar, int parity, const Abort& ab) const {
+    return warp_wait(sbar + 8 * bar, parity & 1, ab);
+  }
+};
+
+// Separate P (d = 64): S_t(j+1) is issued once S_t(j) has been read, P_t(j) V_j once P_t(j) is written.
+template <int D>
+__device__ __forceinline__ bool mma_loop_separate_p(const int (&n)[2], const MmaCtx<D>& m, const Abort& ab) {
+  using C = Cfg<D>;
   const int nmax = max(n[0], n[1]);
-  for (int j = 0; j <= nmax && ok; ++j) {
-    int kslot = 0, vslot = 0;
-    if (j < nmax) {
-      const int idx = 2 * j;
-      kslot = idx % C::kSlots;
-      if (!thread_wait(sbar + 8 * (C::kKVFull + kslot), (idx / C::kSlots) & 1, ab)) {
-        ok = false;
-        break;
+  if (nmax == 0) return true;
+  if (!m.wait_kv(0, ab)) return false;
+  tc_fence_after();
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    if (n[t] > 0) {
+      m.issue_s(t, 0);
+      m.commit(C::kSFull + t);
+    }
+  }
+  m.commit(C::kKVEmpty + 0);  // K_0 (slot 0) is free once both S(0) are done
+  for (int j = 0; j < nmax; ++j) {
+    if (j + 1 < nmax) {
+      const int kidx = 2 * (j + 1);
+      if (!m.wait_kv(kidx, ab)) return false;
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        if (j + 1 < n[t]) {
+          if (!m.wait(C::kSFree + t, j, ab)) return false;
+          tc_fence_after();
+          m.issue_s(t, kidx % C::kSlots);
+          m.commit(C::kSFull + t);
+        }
+      }
+      m.commit(C::kKVEmpty + kidx % C::kSlots);
+    }
+    const int vidx = 2 * j + 1;
+    if (!m.wait_kv(vidx, ab)) return false;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+      if (j < n[t]) {
+        if (!m.wait(C::kPFull + t, j, ab)) return false;
+        tc_fence_after();
+        m.issue_pv(t, vidx % C::kSlots, j == 0);
+        m.commit(C::kPVDone + t);
+        if (j == n[t] - 1) m.commit(C::kOFull + t);
       }
     }
-    if (j > 0) {
-      const int idx = 2 * (j - 1) + 1;
-      vslot = idx % C::kSlots;
-      if (!thread_wait(sbar + 8 * (C::kKVFull + vslot), (idx / C::kSlots) & 1, ab)) {
-        ok = false;
-        break;
-      }
-    }
+    m.commit(C::kKVEmpty + vidx % C::kSlots);
+  }
+  return true;
+}
+
+// P aliased over S (d = 128): S_t(j+1) is issued after P_t(j) V_j, which reads P_t from the same
+// columns (tcgen05.mma operations of one CTA execute in issue order).
+template <int D>
+__device__ __forceinline__ bool mma_loop_aliased_p(const int (&n)[2], const MmaCtx<D>& m, const Abort& ab) {
+  using C = Cfg<D>;
+  const int nmax = max(n[0], n[1]);
+  for (int j = 0; j <= nmax; ++j) {
+    if (j < nmax && !m.wait_kv(2 * j, ab)) return false;
+    if (j > 0 && !m.wait_kv(2 * (j - 1) + 1, ab)) return false;
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
       if (j > 0 && j - 1 < n[t]) {
-        // O_t += P_t(j-1) V_{j-1}: A from TMEM (bf16 pairs packed per column), B = V MN-major.
-        if (!thread_wait(sbar + 8 * (C::kPFull + t), (j - 1) & 1, ab)) {
-          ok = false;
-          break;
-        }
+        if (!m.wait(C::kPFull + t, j - 1, ab)) return false;
         tc_fence_after();
-        const uint32_t v_addr = sbase + C::kKVOff + vslot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, kAtomBytes, 1024);
-          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, bdesc, kIdPV,
-                 (j - 1 > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (j - 1 == n[t] - 1) mma_commit(sbar + 8 * (C::kOFull + t));
+        m.issue_pv(t, (2 * (j - 1) + 1) % C::kSlots, j == 1);
+        if (j - 1 == n[t] - 1) m.commit(C::kOFull + t);
       }
       if (j < n[t]) {
-        // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzled, 16 keys of d per step.
-        const uint32_t q_addr = sbase + C::kQOff + t * C::kTileBytes;
-        const uint32_t k_addr = sbase + C::kKVOff + kslot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          mma_ss(tmem + 128 * t, smem_desc_sw128(q_addr + off, 16, 1024),
-                 smem_desc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(sbar + 8 * (C::kSFull + t));
+        m.issue_s(t, (2 * j) % C::kSlots);
+        m.commit(C::kSFull + t);
       }
     }
-    if (!ok) break;
-    if (j < nmax) mma_commit(sbar + 8 * (C::kKVEmpty + kslot));
-    if (j > 0) mma_commit(sbar + 8 * (C::kKVEmpty + vslot));
+    if (j < nmax) m.commit(C::kKVEmpty + (2 * j) % C::kSlots);
+    if (j > 0) m.commit(C::kKVEmpty + (2 * (j - 1) + 1) % C::kSlots);
   }
-  if (!ok) {
-    // Make sure no MMA is still writing tensor memory when it is freed.
-    mma_commit(sbar + 8 * C::kDrain);
-    volatile uint32_t never = 0;
-    mbar_wait_bounded(sbar + 8 * C::kDrain, 0, &never, globaltimer_ns() + 50ull * 1000 * 1000);
-  }
+  return true;
+}
+
+// Whole warp.
+template <int D>
+__device__ __forceinline__ void mma_role(const int (&n)[2], uint32_t tmem, uint32_t sbase, const Abort& ab) {
+  using C = Cfg<D>;
+  MmaCtx<D> m;
+  m.init(tmem, sbase);
+  bool ok = true;
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t)
+    if (n[t] > 0 && ok) ok = m.wait(C::kQFull + t, 0, ab);
+  if (ok) ok = C::kSepP ? mma_loop_separate_p<D>(n, m, ab) : mma_loop_aliased_p<D>(n, m, ab);
+  // Before the CTA winds down, every MMA (and every arrival its commits make on this CTA's
+  // barriers) has completed, on the normal path and after a timeout alike.
+  m.commit(C::kDrain);
+  volatile uint32_t never = 0;
+  const uint64_t until = ok ? ab.deadline : globaltimer_ns() + 50ull * 1000 * 1000;
+  mbar_wait_bounded(m.sbar + 8 * C::kDrain, 0, &never, until);
+  __syncwarp();
 }
 
 template <int D>
@@ -394,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(sbar + 8 * (C::kQFull + t), 1);
       mbar_init(sbar + 8 * (C::kSFull + t), 1);
-      mbar_init(sbar + 8 * (C::kPFull + t), kBlockM);
+      mbar_init(sbar + 8 * (C::kSFree + t), kBlockM / 32);  // one arrival per softmax warp
+      mbar_init(sbar + 8 * (C::kPFull + t), kBlockM / 32);
+      mbar_init(sbar + 8 * (C::kPVDone + t), 1);
       mbar_init(sbar + 8 * (C::kOFull + t), 1);
     }
     mbar_init(sbar + 8 * C::kDrain, 1);
@@ -422,8 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, n, row0, bh, sbase, ab);
     __syncwarp();
   } else {
-    if ((threadIdx.x & 31) == 0) mma_role<D>(n, tmem, sbase, ab);
-    __syncwarp();
+    mma_role<D>(n, tmem, sbase, ab);
   }
 
   tc_fence_before();
