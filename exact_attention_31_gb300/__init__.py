@@ -17,6 +17,7 @@ __all__ = [
     "FattnError",
     "fattn_fwd",
     "fattn_decode",
+    "fattn_decode_static",
     "fattn_decode_num_splits",
     "fattn_decode_workspace_size",
     "fattn_last_error",
@@ -60,6 +61,8 @@ def lib() -> ctypes.CDLL:
     L.fattn_decode_workspace_size.restype = sz
     L.fattn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     L.fattn_decode.restype = i
+    L.fattn_decode_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    L.fattn_decode_static.restype = i
     L.fattn_last_error.argtypes = [vp]
     L.fattn_last_error.restype = i
     L.fattn_status_string.argtypes = [i]
@@ -173,6 +176,37 @@ def fattn_decode(q, k_cache, v_cache, scale: float | None = None, num_splits: in
                             _stream_handle(stream, q.device))
     if st != FATTN_OK:
         raise FattnError(st, "fattn_decode")
+    return out, lse
+
+
+def fattn_decode_static(q, k_cache, v_cache, scale: float | None = None, num_splits: int = 0, out=None,
+                        lse=None, stream=None, want_lse: bool = True):
+    """fattn_decode without a workspace, for callers that must not allocate device memory: the
+    partial states go to a fixed array inside the library (FATTN_DECODE_STATIC_WORKSPACE_BYTES per
+    device).  Calls whose GPU work overlaps race on that array.  Outputs are allocated here only when
+    not passed in.  Returns (out, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16)
+    if q.dim() != 4 or q.shape[2] != 1 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected q [B,H,1,d] and k/v caches [B,H,Nk,d]")
+    B, H, _, d = q.shape
+    if k_cache.shape[0] != B or k_cache.shape[1] != H or k_cache.shape[3] != d:
+        raise ValueError("q and the caches disagree on B, H or d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32)
+    st = lib().fattn_decode_static(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None, B, H, k_cache.shape[2], d,
+                                   float(scale), int(num_splits), _stream_handle(stream, q.device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_decode_static")
     return out, lse
 
 

@@ -173,6 +173,76 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
   return FATTN_OK;
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free decode: the partial states live in a fixed array compiled into the library.
+// ------------------------------------------------------------------------------------------------
+namespace fattn {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_static_ws[FATTN_DECODE_STATIC_WORKSPACE_BYTES];
+
+// The array's host-side name is only a stand-in for the symbol; the kernels need its device
+// address, looked up once per device with that device current.
+cudaError_t decode_static_ws_ptr(void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && cache[dev] != nullptr) {
+    *out = cache[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_static_ws);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = p;
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace fattn
+
+extern "C" {
+
+fattn_status fattn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                 float* lse, int B, int H, int Nk, int d, float scale, int num_splits,
+                                 void* stream) {
+  if (!q || !k_cache || !v_cache || !o) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nk, 1)) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const size_t cap = FATTN_DECODE_STATIC_WORKSPACE_BYTES;
+  int S = fattn_decode_num_splits(Nk, num_splits);
+  if (S < 1) return FATTN_ERR_INVALID_ARG;
+  if (num_splits == 0) {
+    // largest split count (at most one per 64-key block) whose partial states fit
+    while (S > 1 && fattn_decode_workspace_size(B, H, Nk, d, S) > cap) {
+      const size_t per_split = static_cast<size_t>(B) * H * (d + 2) * sizeof(float);
+      const int guess = static_cast<int>(cap / per_split);
+      S = (guess >= 1 && guess < S) ? guess : S - 1;
+    }
+  }
+  const size_t need = fattn_decode_workspace_size(B, H, Nk, d, S);
+  if (need == 0 || need > cap) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * S > 0x7fffffffLL) return FATTN_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  if (decode_static_ws_ptr(&ws) != cudaSuccess) return FATTN_ERR_CUDA;
+  const size_t parts = static_cast<size_t>(B) * H * S;
+  float* ws_o = static_cast<float*>(ws);
+  float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(parts * d * sizeof(float), 256));
+  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml};
+  if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
 fattn_status fattn_last_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;

@@ -103,6 +103,37 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
                           size_t workspace_bytes, void* stream);
 
 /*
+ * fattn_decode_static -- fattn_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point: it exists for users of this library who are
+ * handed only their inputs, outputs and a stream and may not call cudaMalloc -- for example a
+ * plugin inside a host framework that owns every device allocation, or a latency-critical path
+ * where an allocation's implicit device synchronisation is not acceptable.  It computes the same
+ * result as fattn_decode with the same arguments, minus the workspace: the partial (m, l, O)
+ * states live in a fixed scratch array compiled into the library (FATTN_DECODE_STATIC_WORKSPACE_BYTES
+ * of device memory on every GPU that loads the library, held until the process exits).  Nothing is
+ * allocated, by this library or by any library it calls.
+ *
+ *   num_splits  0 picks the largest split count, at most one per 64-key block, whose partial
+ *               states fit in the array; an explicit count must fit in the array too.
+ *   Returns FATTN_ERR_INVALID_ARG, launching nothing, when the partial states for these sizes do
+ *   not fit (B * H * num_splits * (d + 2) floats, each of the two arrays rounded up to 256 bytes,
+ *   must not exceed FATTN_DECODE_STATIC_WORKSPACE_BYTES; with num_splits = 0 this only fails when
+ *   a single split per (b, h) does not fit).  The other arguments are checked as in fattn_decode.
+ *
+ * Set-up: the first call on each device looks up the device address of the array, with that
+ * device current; make that first call before any stream capture begins.
+ * Sharing: every call on a device uses the same array and leaves its contents behind.  No part of
+ * it needs clearing: each call writes every partial state it later reads.  Two calls whose work
+ * overlaps on the GPU (different streams, or other host threads) race on the array and may return
+ * wrong results; serialise them.
+ */
+#define FATTN_DECODE_STATIC_WORKSPACE_BYTES (8u << 20)
+fattn_status fattn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                 float* lse, int B, int H, int Nk, int d, float scale, int num_splits,
+                                 void* stream);
+
+/*
  * fattn_last_error -- wait for `stream`, then read and clear the library's on-device status word on
  * the current device.  Returns FATTN_OK, FATTN_ERR_TIMEOUT if some kernel's bounded wait gave up
  * since the last read (its outputs are then unspecified), or FATTN_ERR_CUDA if the stream reported
