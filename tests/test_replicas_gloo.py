@@ -1,0 +1,47 @@
+"""The N > 1 path of bench.py on CPU: two gloo ranks, replicas only (no data-path collective).
+
+Each rank reports its own step time; the job time is the maximum over ranks, and the throughput
+counts the units every rank processed.
+"""
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    w, r, local = bench.dist_env()
+    assert (w, r, local) == (world, rank, rank)
+    dist = bench.init_dist(w, "gloo")
+    try:
+        t = bench.max_over_ranks(1.5 + rank, dist, "cpu")
+        dist.barrier()
+        out[rank] = t
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.init_dist(1, "gloo") is None
+    assert bench.max_over_ranks(3.0, None, "cpu") == 3.0
