@@ -31,6 +31,16 @@ unsigned long long wait_timeout_ns() {
   return ns;
 }
 
+// Failure-detection testing only: FATTN_TEST_DROP_KV_BLOCK=<j> makes the prefill kernel skip the
+// load of key tile j, so that its bounded waits give up and report FATTN_ERR_TIMEOUT.
+int test_drop_kv_block() {
+  static int j = [] {
+    const char* s = getenv("FATTN_TEST_DROP_KV_BLOCK");
+    return s ? atoi(s) : -1;
+  }();
+  return j;
+}
+
 // Device address of g_device_status for the current device, looked up once per device.
 cudaError_t device_status_ptr(unsigned int** out) {
   static std::mutex mu;
@@ -126,7 +136,7 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
-  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale};
+  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, test_drop_kv_block()};
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;

@@ -21,6 +21,9 @@ struct FwdProblem {
   float* lse;
   int B, H, Nq, Nk, d, causal;
   float scale;
+  // Failure-detection testing only (never set in normal use): the key tile of this block index is
+  // not loaded, so the waits for it must give up and report a timeout.  -1 = off.
+  int drop_kv_block;
 };
 
 struct DecodeProblem {

@@ -84,6 +84,7 @@ struct Args {
   float c_log2;        // scale * log2(e)
   unsigned int* status;
   unsigned long long timeout_ns;
+  int drop_kv_block;  // failure-detection testing only; -1 = off
 };
 
 // Number of key/value tiles query tile [r0, r0 + 128) must visit (0 if the tile is past Nq).
@@ -325,7 +326,7 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
 template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk,
                                               const CUtensorMap* tv, const int (&n)[2], int row0,
-                                              int bh, uint32_t sbase, const Abort& ab) {
+                                              int bh, uint32_t sbase, int drop_kv_block, const Abort& ab) {
   using C = Cfg<D>;
   const uint32_t sbar = sbase + C::kBarOff;
   tma_prefetch_desc(tq);
@@ -342,7 +343,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
                   row0 + t * kBlockM, bh);
   }
   const int nmax = max(n[0], n[1]);
-  int issued = 0;
+  int issued = 0;   // ring index one past the last load issued
+  int dropped = -1; // ring index of the load skipped for failure-detection testing
   bool ok = true;
   for (int j = 0; j < nmax && ok; ++j) {
 #pragma unroll
@@ -354,13 +356,17 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
         ok = false;
         break;
       }
+      issued = idx + 1;
+      if (w == 0 && j == drop_kv_block) {  // testing only: this tile never arrives
+        dropped = idx;
+        continue;
+      }
       const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
       mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
       for (int ch = 0; ch < C::kChunks; ++ch)
         tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + ch * kAtomBytes, w ? tv : tk, bar,
                     ch * 64, j * kBlockN, bh);
-      ++issued;
     }
   }
   if (!ok) {
@@ -368,6 +374,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
     const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
     volatile uint32_t never = 0;
     for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx) {
+      if (idx == dropped) continue;
       const int slot = idx % C::kSlots;
       mbar_wait_bounded(sbar + 8 * (C::kKVFull + slot), (idx / C::kSlots) & 1, &never, until);
     }
@@ -579,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;
     softmax_role<D>(t, n[t], row0, bh, tmem, sbar, a, ab);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, n, row0, bh, sbase, ab);
+    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, n, row0, bh, sbase, a.drop_kv_block, ab);
     __syncwarp();
   } else {
     mma_role<D>(n, tmem, sbase, ab);
@@ -619,6 +626,7 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.c_log2 = p.scale * 1.4426950408889634f;
   a.status = status;
   a.timeout_ns = timeout_ns;
+  a.drop_kv_block = p.drop_kv_block;
   const unsigned int grid = static_cast<unsigned int>(a.units_per_head) * static_cast<unsigned int>(a.BH);
   prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();

@@ -1,0 +1,53 @@
+"""Failure detection without a GPU fault.
+
+Every wait in the prefill kernel is bounded.  A wait that gives up sets the library's device
+status word, and the kernel then winds down: in-flight copies land, MMAs drain, TMEM is freed.
+The host reads the word with fattn_last_error.  The test makes one wait run out: a test-only switch
+(FATTN_TEST_DROP_KV_BLOCK) stops the producer from loading one key tile, so nothing ever completes
+that tile's barrier.  The test then checks that the call returns, that the timeout is reported
+exactly once, and that the context is still usable.  It runs in a child process because the
+switches are read once per process.
+"""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import math, sys
+sys.path.insert(0, sys.argv[1])
+sys.path.insert(0, sys.argv[1] + "/tests")
+import numpy as np
+import torch
+import exact_attention_31_gb300 as fa
+from exact_attention_31_gb300.workloads import make_qkv
+from parity_utils import compare, oracle_full
+
+q, k, v, _ = make_qkv(1, 2, 512, 512, 64, seed=7, device="cuda")
+o, lse = fa.fattn_fwd(q, k, v)          # key tile 1 is never loaded
+torch.cuda.synchronize()                # the kernel ended by itself; no CUDA error
+assert fa.fattn_last_error() == fa.FATTN_ERR_TIMEOUT
+assert fa.fattn_last_error() == fa.FATTN_OK   # read-and-clear
+
+# the context is still usable and correct
+dq, dk, dv, _ = make_qkv(1, 2, 1, 300, 64, seed=8, device="cuda")
+od, ld = fa.fattn_decode(dq, dk, dv)
+torch.cuda.synchronize()
+o_ref, l_ref = oracle_full(dq, dk, dv, False, 1 / math.sqrt(64))
+compare(od, ld, o_ref, l_ref, what="decode after a reported timeout")
+assert fa.fattn_last_error() == fa.FATTN_OK
+print("FAILURE-DETECTION-OK")
+"""
+
+
+@pytest.mark.gpu
+def test_bounded_wait_reports_timeout_and_context_survives():
+    env = dict(os.environ, FATTN_WAIT_TIMEOUT_MS="200", FATTN_TEST_DROP_KV_BLOCK="1")
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "FAILURE-DETECTION-OK" in r.stdout
