@@ -13,9 +13,10 @@
 // the split the sub-streams are merged with the same correction rule and written as one partial
 // (m, l, O[d]).
 //
-// Combine kernel: one CTA per (b, h) merges its partials: M = max m_s, w_s = exp(m_s - M),
-// l = sum w_s l_s, O = sum w_s O_s / l, L = M + log(l) ("Flash Attention: The Hidden Gem", The
-// Correction Factor; exact by exp(a-c) = exp(a-b) exp(b-c)).
+// Combine kernel: one CTA per (b, h) merges its partials to M = max m_s, l = sum exp(m_s - M) l_s,
+// O = sum exp(m_s - M) O_s / l, L = M + log(l) ("Flash Attention: The Hidden Gem", The Correction
+// Factor), pairwise with the same rule so that no separate pass for M is needed (exact by
+// exp(a-c) = exp(a-b) exp(b-c)).
 //
 // All exponents are base 2 on scores pre-multiplied by c = scale * log2(e).
 #include <cuda_bf16.h>
@@ -28,7 +29,7 @@ namespace fattn {
 namespace {
 
 constexpr int kSplitWarps = 4;           // warps per CTA in the split kernel
-constexpr int kCombineThreads = 128;
+constexpr int kCombineThreads = 256;
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
@@ -164,61 +165,67 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
   }
 }
 
+// Merge of partial states (m_a, l_a, acc_a) <- (m_b, l_b, acc_b) by the correction-factor rule.
+__device__ __forceinline__ void merge_state(float& m, float& l, float4& acc, float mb, float lb, float4 ob) {
+  const float mm = fmaxf(m, mb);
+  const float wa = (mm == -INFINITY) ? 0.f : ex2_approx(m - mm);
+  const float wb = (mm == -INFINITY) ? 0.f : ex2_approx(mb - mm);
+  l = fmaf(l, wa, lb * wb);
+  acc.x = fmaf(acc.x, wa, ob.x * wb);
+  acc.y = fmaf(acc.y, wa, ob.y * wb);
+  acc.z = fmaf(acc.z, wa, ob.z * wb);
+  acc.w = fmaf(acc.w, wa, ob.w * wb);
+  m = mm;
+}
+
+// One CTA per (b, h).  D/4 threads cover one partial O_s (a float4 each); the CTA's groups of D/4
+// threads walk the splits in one pass, each keeping its own running (m, l, O) and loading
+// kUnroll partial states ahead, then the groups' states are merged through shared memory.
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads)
     decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int S) {
   constexpr int kLanesPerRow = D / 4;                       // float4 per thread
   constexpr int kGroups = kCombineThreads / kLanesPerRow;   // splits handled in parallel
-  __shared__ float red[kCombineThreads / 32];
+  constexpr int kUnroll = 4;
   __shared__ float4 part_acc[kGroups][kLanesPerRow];
-  __shared__ float part_l[kGroups];
+  __shared__ float2 part_ml[kGroups];
   const int bh = blockIdx.x;
   const int tid = threadIdx.x;
-  const float* ml = ws_ml + static_cast<size_t>(bh) * S * 2;
-
-  float M = -INFINITY;
-  for (int s = tid; s < S; s += kCombineThreads) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if ((tid & 31) == 0) red[tid >> 5] = M;
-  __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
-
   const int g = tid / kLanesPerRow, c = tid % kLanesPerRow;
+  const float2* ml = reinterpret_cast<const float2*>(ws_ml) + static_cast<size_t>(bh) * S;
+  const float* base = ws_o + static_cast<size_t>(bh) * S * D + 4 * c;
+
+  float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-  const float* base = ws_o + static_cast<size_t>(bh) * S * D;
-  for (int s = g; s < S; s += kGroups) {
-    const float w = ex2_approx(ml[2 * s] - M);
-    lsum = fmaf(w, ml[2 * s + 1], lsum);
-    const float4 x = *reinterpret_cast<const float4*>(base + static_cast<size_t>(s) * D + 4 * c);
-    acc.x = fmaf(w, x.x, acc.x);
-    acc.y = fmaf(w, x.y, acc.y);
-    acc.z = fmaf(w, x.z, acc.z);
-    acc.w = fmaf(w, x.w, acc.w);
+  for (int s0 = g; s0 < S; s0 += kGroups * kUnroll) {
+    float2 st[kUnroll];
+    float4 ov[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s0 + u * kGroups;
+      if (s < S) {
+        st[u] = ml[s];
+        ov[u] = *reinterpret_cast<const float4*>(base + static_cast<size_t>(s) * D);
+      } else {
+        st[u] = make_float2(-INFINITY, 0.f);
+        ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) merge_state(m, l, acc, st[u].x, st[u].y, ov[u]);
   }
   part_acc[g][c] = acc;
-  if (c == 0) part_l[g] = lsum;
+  if (c == 0) part_ml[g] = make_float2(m, l);
   __syncthreads();
   if (g == 0) {
-    float L = part_l[0];
 #pragma unroll
-    for (int gg = 1; gg < kGroups; ++gg) {
-      const float4 y = part_acc[gg][c];
-      acc.x += y.x;
-      acc.y += y.y;
-      acc.z += y.z;
-      acc.w += y.w;
-      L += part_l[gg];
-    }
-    const float inv = 1.f / L;
+    for (int gg = 1; gg < kGroups; ++gg) merge_state(m, l, acc, part_ml[gg].x, part_ml[gg].y, part_acc[gg][c]);
+    const float inv = 1.f / l;
     const uint32_t lo = pack_bf16x2(acc.x * inv, acc.y * inv);
     const uint32_t hi = pack_bf16x2(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(o + static_cast<size_t>(bh) * D + 4 * c) = make_uint2(lo, hi);
-    if (c == 0 && lse != nullptr) lse[bh] = (M + __log2f(L)) * 0.6931471805599453f;
+    if (c == 0 && lse != nullptr) lse[bh] = (m + __log2f(l)) * 0.6931471805599453f;
   }
 }
 
