@@ -12,6 +12,7 @@ Pages cited by the functions below:
   "Flash Attention: The Hidden Gem" -- safe softmax, online softmax, the forward algorithm, L.
   "FlashAttention: attention was never compute-bound" -- online softmax demo 2 and its broken
   no-rescale variant.
+  "Flash Attention: The Hidden Gem", Phase 2 -- the gradients dQ, dK, dV (softmax Jacobian).
   "Understanding FlashAttention" -- the online normalizer (g, s) and the attention shapes.
 """
 
@@ -68,6 +69,9 @@ def _load():
         lib.oracle_attention_probs.argtypes = [_D, _D] + [ctypes.c_int64] * 3 + [
             ctypes.c_int, ctypes.c_double, _D]
         lib.oracle_attention_probs.restype = None
+        lib.oracle_attention_backward.argtypes = [_D] * 7 + [ctypes.c_int64] * 5 + [
+            ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.oracle_attention_backward.restype = None
         _lib = lib
         return lib
 
@@ -167,3 +171,22 @@ def attention_probs(q, k, causal: bool = False, scale: float | None = None) -> n
     p = np.empty((Nq, Nk), dtype=np.float64)
     _load().oracle_attention_probs(_p(q), _p(k), Nq, Nk, d, 1 if causal else 0, float(scale), _p(p))
     return p
+
+
+def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = None,
+                       nthreads: int | None = None):
+    """Gradients (dq, dk, dv) of O = softmax(scale*QK^T + mask) V for an upstream gradient do,
+    by definition ("Flash Attention: The Hidden Gem", Phase 2), with the factor scale on dq and dk
+    from X = scale * Q K^T.  Shapes as in attention(); returns float64 arrays."""
+    q, k, v, B, H, Nq, Nk, d = _shape4(q, k, v)
+    do = _f64(do)
+    if do.shape != q.shape:
+        raise ValueError("do must have q's shape")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    _load().oracle_attention_backward(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv), B, H, Nq, Nk, d,
+                                      1 if causal else 0, float(scale), nthreads or default_threads())
+    return dq, dk, dv

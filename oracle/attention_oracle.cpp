@@ -224,4 +224,60 @@ void oracle_attention_probs(const double* q, const double* k, int64_t Nq, int64_
     }
 }
 
+// Gradients of attention by its definition ("Flash Attention: The Hidden Gem", Phase 2: Gradient
+// and the Jacobian, Chain Rule Through a Matrix Multiply, The Softmax Jacobian).  With
+// P = softmax(X + mask), X = scale * Q K^T, O = P V and an upstream gradient dO:
+//   dV = P^T dO,  dP = dO V^T,  dX_ij = P_ij (dP_ij - D_i)  with  D_i = sum_k dP_ik P_ik,
+//   dQ = scale * dX K,  dK = scale * dX^T Q.
+// D is computed from the Jacobian form (rowsum(dP o P)), not from the rowsum(dO o O) shortcut, so
+// that the shortcut can be checked against it.  The pages write the backward without the scale;
+// the factor scale on dQ and dK is the chain rule through X = scale * Q K^T.
+//   q, dq: [B,H,Nq,d]; k, v, dk, dv: [B,H,Nk,d]; do_: [B,H,Nq,d]; fp64, row-major.
+// Heads are independent and run in parallel.  Masked entries have P = 0, hence dX = 0.
+void oracle_attention_backward(const double* q, const double* k, const double* v, const double* do_,
+                               double* dq, double* dk, double* dv, int64_t B, int64_t H, int64_t Nq,
+                               int64_t Nk, int64_t d, int causal, double scale, int nthreads) {
+  parallel_for(B * H, nthreads, [&](int64_t bh) {
+    const double* Q = q + bh * Nq * d;
+    const double* K = k + bh * Nk * d;
+    const double* V = v + bh * Nk * d;
+    const double* dO = do_ + bh * Nq * d;
+    double* dQ = dq + bh * Nq * d;
+    double* dK = dk + bh * Nk * d;
+    double* dV = dv + bh * Nk * d;
+    std::vector<double> P(static_cast<size_t>(Nq * Nk));
+    oracle_attention_probs(Q, K, Nq, Nk, d, causal, scale, P.data());
+    for (int64_t x = 0; x < Nk * d; ++x) {
+      dK[x] = 0.0;
+      dV[x] = 0.0;
+    }
+    std::vector<double> dP(static_cast<size_t>(Nk));
+    std::vector<double> dX(static_cast<size_t>(Nk));
+    for (int64_t i = 0; i < Nq; ++i) {
+      const double* p = P.data() + i * Nk;
+      // dV += P^T dO (row i's contribution)
+      for (int64_t j = 0; j < Nk; ++j)
+        for (int64_t t = 0; t < d; ++t) dV[j * d + t] += p[j] * dO[i * d + t];
+      // dP_i = dO_i V^T
+      for (int64_t j = 0; j < Nk; ++j) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < d; ++t) acc += dO[i * d + t] * V[j * d + t];
+        dP[j] = acc;
+      }
+      // D_i = sum_k dP_ik P_ik; dX_ij = P_ij (dP_ij - D_i)
+      double Di = 0.0;
+      for (int64_t j = 0; j < Nk; ++j) Di += dP[j] * p[j];
+      for (int64_t j = 0; j < Nk; ++j) dX[j] = p[j] * (dP[j] - Di);
+      // dQ_i = scale * dX_i K;  dK += scale * dX_i^T Q_i
+      for (int64_t t = 0; t < d; ++t) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) acc += dX[j] * K[j * d + t];
+        dQ[i * d + t] = scale * acc;
+      }
+      for (int64_t j = 0; j < Nk; ++j)
+        for (int64_t t = 0; t < d; ++t) dK[j * d + t] += scale * dX[j] * Q[i * d + t];
+    }
+  });
+}
+
 }  // extern "C"
