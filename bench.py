@@ -57,6 +57,17 @@ def prefill_bytes(B, H, N, d):
     return B * H * N * d * 2 * 4 + B * H * N * 4
 
 
+def backward_flops(B, H, N, d, causal):
+    # the five products of the backward (S, dP, dV, dK, dQ), 2*N*N*d each; half under the causal mask
+    f = 10.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def backward_bytes(B, H, N, d):
+    # read Q, K, V, O, dO (bf16) and L; write dQ, dK, dV (bf16)
+    return B * H * N * d * 2 * 8 + B * H * N * 4
+
+
 def decode_kv_bytes(B, H, Nk, d):
     return 2 * B * H * Nk * d * 2
 
@@ -459,6 +470,95 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_backward(args):
+    """Time fattn_bwd (pre-pass, fused kernel, dQ pass) on the prefill workload's shape.  This is a
+    line of its own, outside the benchmark step: the step is the forward hot path."""
+    import torch
+    world, rank, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_31_gb300 as fa
+    from exact_attention_31_gb300.workloads import make_dout, make_qkv
+    fa.lib()
+    P = dict(PREFILL, H=args.prefill_heads or PREFILL["H"], d=args.bwd_d or PREFILL["d"])
+    B, H, N, d = P["B"], P["H"], P["N"], P["d"]
+    seed = 0xFA77E000 + 4
+    stream = torch.cuda.current_stream(dev)
+    scale = 1 / math.sqrt(d)
+    q, k, v, _ = make_qkv(B, H, N, N, d, seed, dev)
+    do = make_dout(B, H, N, d, seed, dev)
+    o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=scale, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fattn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        flush.zero_()
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fattn_bwd(q, k, v, o, lse, do, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                     stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for_smi(dev)).start() if args.clocks else None
+    if sampler is not None:
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    if sampler is not None:
+        time.sleep(0.15)
+        sampler.stop()
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    avg = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, dist, dev)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    fl = backward_flops(B, H, N, d, True)
+    tf = fl / (avg * 1e-3) / 1e12
+    line = {
+        "metric": "attn bwd TFLOP/s (fattn_bwd: pre-pass + fused kernel + dQ pass)",
+        "value": round(world * tf, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded iid N(0,1) drawn in fp32 and rounded to bf16 (q, k, v, dO)",
+        "config": {"workload": f"backward_b{B}h{H}_n{N}_d{d} causal",
+                   "backward": {"B": B, "H": H, "Nq": N, "Nk": N, "d": d, "causal": True, "scale": scale,
+                                "flops_per_call": fl},
+                   "l2": "a 512 MiB buffer is written before every call (outside the per-call events)",
+                   "parallelism": f"replicas x{world}"},
+        "bwd_ms": round(avg, 4),
+        "roofline": {"kernel": f"fattn_bwd (bwd_prep_kernel<{d}> + bwd_kernel<{d}> + bwd_dq_kernel<{d}>)",
+                     "bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM)", "traffic": None,
+                     "algorithmic_bytes": backward_bytes(B, H, N, d)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(t0, t1) if sampler is not None else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_e2e(fa, dev, stream, args, q, k, v, dq, dk, dv, scale_p, scale_d):
     """The same calls fed from pinned host buffers, copies included in the timing."""
     import torch
@@ -575,8 +675,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
-                    help="both = the benchmark step; the others time one half (used for profiling)")
+    ap.add_argument("--workload", choices=["both", "prefill", "decode", "backward"], default="both",
+                    help="both = the benchmark step; prefill/decode time one half (profiling); backward "
+                         "times fattn_bwd on the prefill shape (a line of its own)")
+    ap.add_argument("--bwd-d", type=int, default=0, help="override d of the backward workload (64 or 128)")
     ap.add_argument("--prefill-heads", type=int, default=0, help="override H of the prefill (profiling)")
     ap.add_argument("--decode-batch", type=int, default=0, help="override B of the decode (profiling)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -590,6 +692,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "backward":
+        run_backward(args)
     else:
         run_ours(args)
 

@@ -1,7 +1,8 @@
 """exact_attention_31_gb300 -- exact fused attention for GB300 (sm_103a), Python binding.
 
-The compute lives in ``libfattn.so`` (hand-written CUDA: a tcgen05/TMEM/TMA prefill kernel, and a
-split-KV decode kernel with its combine kernel) behind the C ABI in ``include/fattn.h``.  This
+The compute lives in ``libfattn.so`` (hand-written CUDA: a tcgen05/TMEM/TMA prefill kernel, its
+backward, and a split-KV decode kernel with its combine kernel) behind the C ABI in
+``include/fattn.h``.  This
 module only marshals torch tensors into that ABI: it checks dtypes, devices and shapes, allocates
 outputs with torch when the caller does not pass them, and raises on a non-OK status.  There is no
 other implementation behind these names: if the library is missing, every call raises.
@@ -16,6 +17,8 @@ import os
 __all__ = [
     "FattnError",
     "fattn_fwd",
+    "fattn_bwd",
+    "fattn_bwd_workspace_size",
     "fattn_decode",
     "fattn_decode_static",
     "fattn_decode_num_splits",
@@ -55,6 +58,10 @@ def lib() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     L.fattn_fwd.restype = i
+    L.fattn_bwd_workspace_size.argtypes = [i, i, i, i]
+    L.fattn_bwd_workspace_size.restype = sz
+    L.fattn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, sz, vp]
+    L.fattn_bwd.restype = i
     L.fattn_decode_num_splits.argtypes = [i, i]
     L.fattn_decode_num_splits.restype = i
     L.fattn_decode_workspace_size.argtypes = [i, i, i, i, i]
@@ -129,6 +136,50 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     if st != FATTN_OK:
         raise FattnError(st, "fattn_fwd")
     return out, lse
+
+
+def fattn_bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
+    return lib().fattn_bwd_workspace_size(int(B), int(H), int(Nq), int(d))
+
+
+def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,
+              dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the attention forward for an upstream gradient ``dout``.
+
+    q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; out (bf16) and lse (fp32 [B,H,Nq]) are the forward's
+    outputs for the same inputs, mask and scale.  ``workspace`` is a CUDA uint8 tensor of at least
+    fattn_bwd_workspace_size(B, H, Nq, d) bytes (allocated here if omitted).  Returns bf16 tensors.
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check(t, n, torch.bfloat16)
+    _check(lse, "lse", torch.float32)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or out.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("expected q, out, dout [B,H,Nq,d] and k, v [B,H,Nk,d]")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q and k/v disagree on B, H or d")
+    if tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("lse must be [B,H,Nq]")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = fattn_bwd_workspace_size(B, H, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16)
+    st = lib().fattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                         1 if causal else 0, float(scale), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_bwd")
+    return dq, dk, dv
 
 
 def fattn_decode_num_splits(Nk: int, num_splits: int = 0) -> int:

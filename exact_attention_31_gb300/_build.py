@@ -1,6 +1,6 @@
 """Build libfattn.so in-tree with nvcc for sm_103a (no cmake, no torch extension machinery).
 
-The three translation units are compiled in parallel and linked into one shared library that
+The translation units are compiled in parallel and linked into one shared library that
 exports the C ABI declared in include/fattn.h.
 """
 
@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 
-SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "decode_sm103a.cu"]
+SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu"]
 HEADERS = ["fattn_internal.h", "sm103a_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,759 @@
+// backward_sm103a.cu -- attention backward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes is the FlashAttention-2 backward pass ("Flash Attention: The Hidden Gem",
+// Phase 2).  Given Q, K, V, the forward's L (log-sum-exp per query row) and O, and the upstream
+// gradient dO:
+//   D   = rowsum(dO o O)                              (The D Shortcut)
+//   P   = exp(scale * Q K^T - L)                      (recomputed from L, The Algorithm step 11)
+//   dV  = P^T dO,  dP = dO V^T                        (Chain Rule Through a Matrix Multiply)
+//   dS  = P o (dP - D)                                (The Softmax Jacobian)
+//   dQ  = scale * dS K,  dK = scale * dS^T Q          (the scale comes from S = scale * Q K^T)
+// with the key/value tile in the outer loop and query tiles in the inner loop (step 5): dK_j and
+// dV_j stay in tensor memory for the whole inner loop and are written once; dQ_i is accumulated in
+// an fp32 array in device memory by every key tile that sees it.
+//
+// Three kernels run in stream order:
+//   bwd_prep_kernel  D_i (stored negated) and -L_i * log2(e) per query row into a padded workspace;
+//                    rows past Nq get (0, -inf) so that their P is exactly 0; zeroes the dQ array
+//   bwd_kernel       one CTA per (head, 128-key tile); walks the query tiles that can see its keys
+//   bwd_dq_kernel    dQ = scale * accumulated array, rounded to bf16
+//
+// bwd_kernel works on transposed tiles so that one thread owns one key: S^T = K Q^T and
+// dP^T = V dO^T land in tensor memory with keys on the 128 lanes and the 128 queries of the tile
+// along the columns.  Thread layout (448 threads):
+//   warps 0-7    compute: warp w reads lanes 32*(w%4).. and the query half w/4 of S^T and dP^T,
+//                forms P^T = exp2(S^T * scale*log2e - L*log2e) and dS^T = P^T o (dP^T - D), writes
+//                P^T (bf16) back into tensor memory and dS^T (bf16) into shared memory
+//   warp  8      TMA producer: K_j and V_j once, then Q_i, dO_i, -L_i*log2e, -D_i per query tile
+//   warp  9      MMA issuer and tensor-memory owner
+//   warps 10-13  dQ drain: one thread per query row reads dQ_i from tensor memory, stages it in
+//                shared memory and adds it into the fp32 array with a TMA reduce
+// The five products per query tile are tcgen05.mma with M = 128:
+//   S^T  = K Q^T        A = K (K-major)          B = Q (K-major)
+//   dP^T = V dO^T       A = V (K-major)          B = dO (K-major)
+//   dV  += P^T dO       A = P^T in TMEM          B = dO read MN-major
+//   dK  += dS^T Q       A = dS^T (K-major)       B = Q read MN-major
+//   dQ   = dS K         A = dS^T read MN-major   B = K read MN-major
+// so one shared-memory copy of dS^T serves both of its products.
+//
+// Tensor memory (512 columns):
+//   d = 64:  S^T buffers at 0 and 128 (two query tiles in flight), dP^T at 256, dV at 384, dK at
+//            448.  After the compute warps have read S^T they overwrite it with P^T packed as bf16
+//            pairs: queries 0-63 in columns 0-31, queries 64-127 in columns 96-127.  Columns 32-95
+//            are then free and receive dQ_i (64 fp32 columns).
+//   d = 128: one S^T buffer at 0, dP^T at 128, dV at 256, dK at 384; dQ_i (128 columns) goes to
+//            the dP^T columns once the compute warps have read them.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fattn_internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace fattn {
+namespace {
+
+constexpr int kBM = 128;  // queries per inner step (columns of S^T)
+constexpr int kBN = 128;  // keys per CTA (TMEM lanes)
+constexpr int kThreads = 448;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDrainWarp0 = 10;
+constexpr int kDrainBarrier = 1;  // named barrier id of the four drain warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes: one swizzled 64-column chunk of a tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BCfg {
+  static constexpr bool kTwoS = (D == 64);
+  static constexpr int kSBufs = kTwoS ? 2 : 1;
+  static constexpr int kStages = kTwoS ? 2 : 1;   // Q_i/dO_i buffers
+  static constexpr int kDSBufs = kTwoS ? 2 : 1;   // dS^T buffers
+  static constexpr int kChunks = D / 64;
+  static constexpr uint32_t kTile = kBM * D * 2;  // one 128-row bf16 tile of Q, K, V or dO
+  static constexpr uint32_t kKOff = 0;
+  static constexpr uint32_t kVOff = kTile;
+  static constexpr uint32_t kStageOff = 2 * kTile;  // stage s: Q at + 2*s*kTile, dO at + (2s+1)*kTile
+  static constexpr uint32_t kDSBytes = kBN * kBM * 2;
+  static constexpr uint32_t kDSOff = kStageOff + kStages * 2 * kTile;
+  static constexpr uint32_t kDQOff = kDSOff + kDSBufs * kDSBytes;  // 64 columns of dQ at a time
+  static constexpr uint32_t kDQBytes = kBM * 64 * 4;
+  static constexpr uint32_t kLDOff = kDQOff + kDQBytes;  // stage s: -L*log2e [128], -D [128]
+  static constexpr uint32_t kBarOff = kLDOff + kStages * 1024;
+  // barrier indices
+  static constexpr int kKVFull = 0;
+  static constexpr int kQFull = 1;    // [2] Q_i, dO_i, -L, -D of a stage landed
+  static constexpr int kQEmpty = 3;   // [2] the stage's last reader (dK_i) done
+  static constexpr int kSFull = 5;    // [2] S^T of a buffer computed
+  static constexpr int kDPFull = 7;   // dP^T computed
+  static constexpr int kCDone = 8;    // compute warps done with a tile (one arrival per warp)
+  static constexpr int kDSEmpty = 9;  // [2] dK_i and dQ_i have read a dS^T buffer
+  static constexpr int kDQFull = 11;  // [2] dQ_i in tensor memory
+  static constexpr int kDQFree = 13;  // [2] dQ_i read out of tensor memory (one arrival per drain warp)
+  static constexpr int kAccDone = 15; // every MMA of the CTA done: dK, dV final
+  static constexpr int kDrain = 16;
+  static constexpr int kNumBars = 17;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // tensor-memory columns
+  __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * b; }
+  static constexpr uint32_t kColDP = kTwoS ? 256u : 128u;
+  static constexpr uint32_t kColDV = kTwoS ? 384u : 256u;
+  static constexpr uint32_t kColDK = kTwoS ? 448u : 384u;
+  __host__ __device__ static constexpr uint32_t col_dq(int b) { return kTwoS ? col_s(b) + 32u : kColDP; }
+};
+
+// Packed P^T columns: queries [64h + 32c, 64h + 32c + 32) of a tile go to 16 columns at this
+// offset from the S^T buffer.  Each compute warp only overwrites columns it has already read.
+__host__ __device__ constexpr uint32_t p_col(int half, int chunk) {
+  return half ? 96u + 16u * chunk : 16u * chunk;
+}
+// ... and 16 queries (K step kk of dV += P^T dO) start at this column.
+__host__ __device__ constexpr uint32_t p_step_col(int kk) { return kk < 4 ? 8u * kk : 96u + 8u * (kk - 4); }
+
+struct BArgs {
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* nl2;   // [BH][Nq_pad]  -L * log2(e)
+  const float* negd;  // [BH][Nq_pad]  -D
+  int BH, Nq, Nk, Nq_pad, NqT, causal, off;
+  float c_log2;  // scale * log2(e)
+  float scale;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+struct Abort {
+  volatile uint32_t* flag;
+  unsigned int* status;
+  uint64_t deadline;
+  __device__ void raise() const {
+    *flag = 1u;
+    atomicOr(status, kStatusTimeout);
+  }
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  bool ok = mbar_wait_bounded(bar, parity, ab.flag, ab.deadline);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) ab.raise();
+  return ok;
+}
+
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  const bool ok = mbar_wait_bounded(bar, parity, ab.flag, ab.deadline);
+  if (!ok) ab.raise();
+  return ok;
+}
+
+__device__ __forceinline__ void wait_dep(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+        "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+        "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+// (o0, o1) = (a0, a1) * b + (c0, c1)
+__device__ __forceinline__ void ffma2(float& o0, float& o1, float a0, float a1, float b, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %6};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(o0), "=f"(o1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+// (o0, o1) = (a0, a1) * ((b0, b1) + (c0, c1))
+__device__ __forceinline__ void fmul_add2(float& o0, float& o1, float a0, float a1, float b0, float b1,
+                                          float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z, t, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
+      "add.rn.f32x2 t, y, z;\n\tmul.rn.f32x2 w, x, t;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(o0), "=f"(o1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// Compute warps: one thread per key; each warp covers 64 of the tile's 128 queries.
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uint32_t tmem, uint32_t sbase,
+                                             const uint8_t* smem, const BArgs& a, const Abort& ab) {
+  using C = BCfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int kr = quarter * 32 + lane;  // key row within the tile = TMEM lane
+  const int kidx = n0 + kr;
+  const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t sbar = sbase + C::kBarOff;
+  const float c = a.c_log2;
+  bool ok = true;
+  for (int i = 0; i < n; ++i) {
+    const int b = i % C::kSBufs;
+    const int st = i % C::kStages;
+    const int dsb = i % C::kDSBufs;
+    if (!warp_wait(sbar + 8 * (C::kSFull + b), (i / C::kSBufs) & 1, ab) ||
+        !warp_wait(sbar + 8 * C::kDPFull, i & 1, ab) ||
+        (i >= C::kDSBufs && !warp_wait(sbar + 8 * (C::kDSEmpty + dsb), ((i / C::kDSBufs) - 1) & 1, ab))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const int q0 = (it0 + i) * kBM;
+    const uint32_t tS = tmem + lane_field + C::col_s(b);
+    const uint32_t tDP = tmem + lane_field + C::kColDP;
+    const float* nl2 = reinterpret_cast<const float*>(smem + C::kLDOff + st * 1024);
+    const float* negd = nl2 + kBM;
+    const uint32_t ds_row = sbase + C::kDSOff + dsb * C::kDSBytes + half * kAtom + kr * 128;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int ch = half ? 1 - cc : cc;  // the upper half writes its packed P^T over chunk 1 first
+      const int qa = 64 * half + 32 * ch;
+      uint32_t s[32], dp[32];
+      tmem_ld_32x32b_x32(tS + qa, s);
+      tmem_ld_32x32b_x32(tDP + qa, dp);
+      wait_dep(s);
+      wait_dep(dp);
+      // Causal: key kidx is visible to query q iff kidx <= q + off.  Elements e < fv of this chunk
+      // are masked.
+      const int fv = a.causal ? kidx - a.off - (q0 + qa) : -1;
+      const bool mask = __any_sync(0xffffffffu, fv > 0);
+      uint32_t pp[16], pd[16];
+#pragma unroll
+      for (int k4 = 0; k4 < 8; ++k4) {
+        const float4 nl = *reinterpret_cast<const float4*>(nl2 + qa + 4 * k4);
+        const float4 nd = *reinterpret_cast<const float4*>(negd + qa + 4 * k4);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int e = 4 * k4 + 2 * hh;
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), c, hh ? nl.z : nl.x,
+                hh ? nl.w : nl.y);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
+          if (mask) {
+            p0 = (e < fv) ? 0.f : p0;
+            p1 = (e + 1 < fv) ? 0.f : p1;
+          }
+          float d0, d1;
+          fmul_add2(d0, d1, p0, p1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), hh ? nd.z : nd.x,
+                    hh ? nd.w : nd.y);
+          pp[e >> 1] = pack_bf16x2(p0, p1);
+          pd[e >> 1] = pack_bf16x2(d0, d1);
+        }
+      }
+      tmem_st_32x32b_x16(tS + p_col(half, ch), pp);
+      // dS^T row kr, queries [qa, qa + 32): 16-byte units 4*ch .. 4*ch + 3 of this half's 128-byte
+      // row, 128-byte swizzled like a TMA tile.
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4(ds_row + ((static_cast<uint32_t>(4 * ch + u) ^ static_cast<uint32_t>(kr & 7)) << 4),
+                     pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sbar + 8 * C::kCDone);
+  }
+  if (!ok) return;
+
+  // Epilogue: dV and scale * dK rows of this warp's keys, this warp's half of the columns.
+  if (!warp_wait(sbar + 8 * C::kAccDone, 0, ab)) return;
+  tc_fence_after();
+  const bool store = kidx < a.Nk;
+  const size_t row = (static_cast<size_t>(bh) * a.Nk + (store ? kidx : 0)) * D;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const uint32_t tcol = tmem + lane_field + (w ? C::kColDK : C::kColDV);
+    __nv_bfloat16* out = (w ? a.dk : a.dv) + row;
+    const float f = w ? a.scale : 1.f;
+#pragma unroll
+    for (int e = 0; e < D / 64; ++e) {
+      const int col = half * (D / 2) + 32 * e;
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tcol + col, r);
+      wait_dep(r);
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * f, __uint_as_float(r[2 * k + 1]) * f);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(out + col);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// TMA producer (one thread)
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                              const CUtensorMap* tdo, int n, int it0, int n0, int bh,
+                                              uint32_t sbase, const BArgs& a, const Abort& ab) {
+  using C = BCfg<D>;
+  const uint32_t sbar = sbase + C::kBarOff;
+  tma_prefetch_desc(tq);
+  tma_prefetch_desc(tk);
+  tma_prefetch_desc(tv);
+  tma_prefetch_desc(tdo);
+  mbar_arrive_expect_tx(sbar + 8 * C::kKVFull, 2 * C::kTile);
+#pragma unroll
+  for (int ch = 0; ch < C::kChunks; ++ch) {
+    tma_load_3d(sbase + C::kKOff + ch * kAtom, tk, sbar + 8 * C::kKVFull, 64 * ch, n0, bh);
+    tma_load_3d(sbase + C::kVOff + ch * kAtom, tv, sbar + 8 * C::kKVFull, 64 * ch, n0, bh);
+  }
+  int issued = 0;
+  bool ok = true;
+  for (int i = 0; i < n; ++i) {
+    const int st = i % C::kStages, use = i / C::kStages;
+    if (use > 0 && !thread_wait(sbar + 8 * (C::kQEmpty + st), (use - 1) & 1, ab)) {
+      ok = false;
+      break;
+    }
+    const int q0 = (it0 + i) * kBM;
+    const uint32_t bar = sbar + 8 * (C::kQFull + st);
+    const uint32_t dst = sbase + C::kStageOff + st * 2 * C::kTile;
+    mbar_arrive_expect_tx(bar, 2 * C::kTile + 2 * kBM * 4);
+#pragma unroll
+    for (int ch = 0; ch < C::kChunks; ++ch) {
+      tma_load_3d(dst + ch * kAtom, tq, bar, 64 * ch, q0, bh);
+      tma_load_3d(dst + C::kTile + ch * kAtom, tdo, bar, 64 * ch, q0, bh);
+    }
+    const size_t r0 = static_cast<size_t>(bh) * a.Nq_pad + q0;
+    bulk_load(sbase + C::kLDOff + st * 1024, a.nl2 + r0, kBM * 4, bar);
+    bulk_load(sbase + C::kLDOff + st * 1024 + kBM * 4, a.negd + r0, kBM * 4, bar);
+    issued = i + 1;
+  }
+  if (!ok) {
+    // Let the copies already in flight land before the CTA's shared memory goes away.
+    const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
+    volatile uint32_t never = 0;
+    mbar_wait_bounded(sbar + 8 * C::kKVFull, 0, &never, until);
+    for (int i = max(0, issued - C::kStages); i < issued; ++i)
+      mbar_wait_bounded(sbar + 8 * (C::kQFull + i % C::kStages), (i / C::kStages) & 1, &never, until);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// MMA issuer: the whole warp runs the schedule, one elected lane issues.
+// ------------------------------------------------------------------------------------------------
+template <int D>
+struct BMma {
+  using C = BCfg<D>;
+  uint32_t tmem, sbar;
+  uint64_t k_kmaj, v_kmaj, k_mn;   // K_j, V_j
+  uint64_t q_kmaj0, do_kmaj0;      // stage 0 Q_i, dO_i as K-major operands
+  uint64_t q_mn0, do_mn0;          // ... and as MN-major operands
+  uint64_t ds_kmaj0, ds_mn0;       // dS^T buffer 0, K-major (for dK) and MN-major (for dQ)
+  uint32_t lead;
+
+  __device__ __forceinline__ void init(uint32_t tmem_, uint32_t sbase) {
+    tmem = tmem_;
+    sbar = sbase + C::kBarOff;
+    k_kmaj = smem_desc_sw128(sbase + C::kKOff, 16, 1024);
+    v_kmaj = smem_desc_sw128(sbase + C::kVOff, 16, 1024);
+    k_mn = smem_desc_sw128(sbase + C::kKOff, kAtom, 1024);
+    q_kmaj0 = smem_desc_sw128(sbase + C::kStageOff, 16, 1024);
+    do_kmaj0 = smem_desc_sw128(sbase + C::kStageOff + C::kTile, 16, 1024);
+    q_mn0 = smem_desc_sw128(sbase + C::kStageOff, kAtom, 1024);
+    do_mn0 = smem_desc_sw128(sbase + C::kStageOff + C::kTile, kAtom, 1024);
+    ds_kmaj0 = smem_desc_sw128(sbase + C::kDSOff, 16, 1024);
+    ds_mn0 = smem_desc_sw128(sbase + C::kDSOff, kAtom, 1024);
+    lead = elect_lane();
+  }
+  // start-address advances, in 16-byte units
+  __host__ __device__ static constexpr uint64_t stage_adv(int st) { return static_cast<uint64_t>(st) * (2 * C::kTile >> 4); }
+  __host__ __device__ static constexpr uint64_t ds_adv(int b) { return static_cast<uint64_t>(b) * (C::kDSBytes >> 4); }
+  // K-major operand, K step kk of 16 elements: 4 steps per 128-byte row, then the next 64-column chunk
+  __host__ __device__ static constexpr uint64_t kmaj_adv(int kk) { return static_cast<uint64_t>((kk >> 2) * kAtom + (kk & 3) * 32) >> 4; }
+  // MN-major operand, K step kk of 16 rows
+  __host__ __device__ static constexpr uint64_t mn_adv(int kk) { return static_cast<uint64_t>(kk * 16 * 128) >> 4; }
+
+  __device__ __forceinline__ void issue_s(int b, int st) const {
+    constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM, false);
+    const uint64_t bq = q_kmaj0 + stage_adv(st);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ss_lead(tmem + C::col_s(b), k_kmaj + kmaj_adv(kk), bq + kmaj_adv(kk), id, kk > 0 ? 1u : 0u, lead);
+  }
+  __device__ __forceinline__ void issue_dp(int st) const {
+    constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM, false);
+    const uint64_t bd = do_kmaj0 + stage_adv(st);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ss_lead(tmem + C::kColDP, v_kmaj + kmaj_adv(kk), bd + kmaj_adv(kk), id, kk > 0 ? 1u : 0u, lead);
+  }
+  __device__ __forceinline__ void issue_dv(int b, int st, bool first) const {
+    constexpr uint32_t id = mma_idesc_bf16_f32(kBN, D, true);
+    const uint64_t bd = do_mn0 + stage_adv(st);
+#pragma unroll
+    for (int kk = 0; kk < kBM / 16; ++kk)
+      mma_ts_lead(tmem + C::kColDV, tmem + C::col_s(b) + p_step_col(kk), bd + mn_adv(kk), id,
+                  (!first || kk > 0) ? 1u : 0u, lead);
+  }
+  __device__ __forceinline__ void issue_dk(int dsb, int st, bool first) const {
+    constexpr uint32_t id = mma_idesc_bf16_f32(kBN, D, true);
+    const uint64_t aa = ds_kmaj0 + ds_adv(dsb), bq = q_mn0 + stage_adv(st);
+#pragma unroll
+    for (int kk = 0; kk < kBM / 16; ++kk)
+      mma_ss_lead(tmem + C::kColDK, aa + kmaj_adv(kk), bq + mn_adv(kk), id, (!first || kk > 0) ? 1u : 0u, lead);
+  }
+  __device__ __forceinline__ void issue_dq(int b, int dsb) const {
+    constexpr uint32_t id = mma_idesc_bf16_f32(kBM, D, true, true);
+    const uint64_t aa = ds_mn0 + ds_adv(dsb);
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+      mma_ss_lead(tmem + C::col_dq(b), aa + mn_adv(kk), k_mn + mn_adv(kk), id, kk > 0 ? 1u : 0u, lead);
+  }
+  __device__ __forceinline__ void commit(int bar) const { mma_commit_lead(sbar + 8 * bar, lead); }
+  __device__ __forceinline__ bool wait(int bar, int parity, const Abort& ab) const {
+    return warp_wait(sbar + 8 * bar, parity & 1, ab);
+  }
+};
+
+template <int D>
+__device__ __forceinline__ bool mma_schedule(int n, const BMma<D>& m, const Abort& ab) {
+  using C = BCfg<D>;
+  if (!m.wait(C::kKVFull, 0, ab) || !m.wait(C::kQFull, 0, ab)) return false;
+  tc_fence_after();
+  m.issue_s(0, 0);
+  m.commit(C::kSFull);
+  m.issue_dp(0);
+  m.commit(C::kDPFull);
+  if (C::kTwoS && n > 1) {
+    if (!m.wait(C::kQFull + 1, 0, ab)) return false;
+    tc_fence_after();
+    m.issue_s(1, 1);
+    m.commit(C::kSFull + 1);
+  }
+  for (int i = 0; i < n; ++i) {
+    const int b = i % C::kSBufs, st = i % C::kStages, dsb = i % C::kDSBufs;
+    if (!m.wait(C::kCDone, i, ab)) return false;
+    tc_fence_after();
+    if constexpr (C::kTwoS) {
+      // dP^T of the next tile first (its dO stage was waited for when its S^T was issued), so its
+      // compute can start while this tile's gradients are accumulated.
+      if (i + 1 < n) {
+        m.issue_dp((i + 1) % C::kStages);
+        m.commit(C::kDPFull);
+      }
+      m.issue_dv(b, st, i == 0);
+      m.issue_dk(dsb, st, i == 0);
+      m.commit(C::kQEmpty + st);
+      m.issue_dq(b, dsb);
+      m.commit(C::kDQFull + b);
+      m.commit(C::kDSEmpty + dsb);
+      if (i + 2 < n) {
+        // S^T of tile i+2 reuses this buffer: after dV_i has read P^T (issue order) and after the
+        // drain warps have read dQ_i out of it.
+        if (!m.wait(C::kDQFree + b, i / 2, ab) || !m.wait(C::kQFull + (i + 2) % C::kStages, (i + 2) / C::kStages, ab))
+          return false;
+        tc_fence_after();
+        m.issue_s(b, (i + 2) % C::kStages);
+        m.commit(C::kSFull + b);
+      }
+    } else {
+      m.issue_dv(0, 0, i == 0);
+      m.issue_dk(dsb, 0, i == 0);
+      m.commit(C::kQEmpty);
+      m.issue_dq(0, dsb);  // into the dP^T columns, read by the compute warps already
+      m.commit(C::kDQFull);
+      m.commit(C::kDSEmpty + dsb);
+      if (i + 1 < n) {
+        if (!m.wait(C::kQFull, i + 1, ab)) return false;
+        tc_fence_after();
+        m.issue_s(0, 0);
+        m.commit(C::kSFull);
+        if (!m.wait(C::kDQFree, i, ab)) return false;
+        tc_fence_after();
+        m.issue_dp(0);
+        m.commit(C::kDPFull);
+      }
+    }
+  }
+  m.commit(C::kAccDone);
+  return true;
+}
+
+template <int D>
+__device__ __forceinline__ void mma_role(int n, uint32_t tmem, uint32_t sbase, const Abort& ab) {
+  using C = BCfg<D>;
+  BMma<D> m;
+  m.init(tmem, sbase);
+  const bool ok = mma_schedule<D>(n, m, ab);
+  // Every MMA (and every arrival its commits make) completes before the CTA winds down.
+  m.commit(C::kDrain);
+  volatile uint32_t never = 0;
+  const uint64_t until = ok ? ab.deadline : globaltimer_ns() + 50ull * 1000 * 1000;
+  mbar_wait_bounded(m.sbar + 8 * C::kDrain, 0, &never, until);
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------------------------------------
+// dQ drain warps: one thread per query row of the tile.
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it0, int bh, uint32_t tmem,
+                                           uint32_t sbase, const Abort& ab) {
+  using C = BCfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t sbar = sbase + C::kBarOff;
+  const bool issuer = (warp == kDrainWarp0) && lane == 0;
+  const uint32_t stg = sbase + C::kDQOff;  // two [128 rows][32 fp32] boxes, 128-byte swizzled
+  if (issuer) tma_prefetch_desc(tdq);
+  for (int i = 0; i < n; ++i) {
+    const int b = i % C::kSBufs;
+    bool fail = !warp_wait(sbar + 8 * (C::kDQFull + b), (i / C::kSBufs) & 1, ab);
+    if (!fail) tc_fence_after();
+    const int q0 = (it0 + i) * kBM;
+#pragma unroll 1
+    for (int pass = 0; pass < D / 64; ++pass) {
+      uint32_t v[2][32];
+      if (!fail) {
+        const uint32_t t = tmem + lane_field + C::col_dq(b) + 64 * pass;
+        tmem_ld_32x32b_x32(t, v[0]);
+        tmem_ld_32x32b_x32(t + 32, v[1]);
+        wait_dep(v[0]);
+        wait_dep(v[1]);
+        if (pass == D / 64 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sbar + 8 * (C::kDQFree + b));
+        }
+      }
+      if (issuer) bulk_wait_read_all();  // the previous reduce has finished reading the staging area
+      fail = named_bar_or(kDrainBarrier, 128, fail);
+      if (fail) break;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t rbase = stg + h * (kBM * 128) + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(rbase + ((static_cast<uint32_t>(u) ^ static_cast<uint32_t>(row & 7)) << 4), v[h][4 * u],
+                       v[h][4 * u + 1], v[h][4 * u + 2], v[h][4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kDrainBarrier, 128);
+      if (issuer) {
+        tma_reduce_add_3d(tdq, stg, 64 * pass, q0, bh);
+        tma_reduce_add_3d(tdq, stg + kBM * 128, 64 * pass + 32, q0, bh);
+        bulk_commit_group();
+      }
+    }
+    if (fail) break;
+  }
+  if (issuer) bulk_wait_all();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_dq, const BArgs a) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const uint32_t sbar = sbase + C::kBarOff;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+
+  // Key tiles with the most query tiles (the first ones, under a causal mask) are launched first.
+  const int jt = static_cast<int>(blockIdx.x) / a.BH;
+  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int n0 = jt * kBN;
+  // Query tiles that can see any of keys [n0, n0 + 128): all of them, or under the causal mask
+  // those with a query q >= n0 - off.  Key n0 < Nk is always visible to query Nq - 1, so n >= 1.
+  const int it0 = a.causal ? max(0, n0 - a.off) / kBM : 0;
+  const int n = a.NqT - it0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(sbar + 8 * C::kKVFull, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sbar + 8 * (C::kQFull + s), 1);
+      mbar_init(sbar + 8 * (C::kQEmpty + s), 1);
+      mbar_init(sbar + 8 * (C::kSFull + s), 1);
+      mbar_init(sbar + 8 * (C::kDSEmpty + s), 1);
+      mbar_init(sbar + 8 * (C::kDQFull + s), 1);
+      mbar_init(sbar + 8 * (C::kDQFree + s), 4);  // one arrival per drain warp
+    }
+    mbar_init(sbar + 8 * C::kDPFull, 1);
+    mbar_init(sbar + 8 * C::kCDone, 8);  // one arrival per compute warp
+    mbar_init(sbar + 8 * C::kAccDone, 1);
+    mbar_init(sbar + 8 * C::kDrain, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  Abort ab{abort_flag, a.status, globaltimer_ns() + a.timeout_ns};
+
+  if (warp < 8) {
+    compute_role<D>(n, it0, n0, bh, tmem, sbase, smem, a, ab);
+  } else if (warp == kProducerWarp) {
+    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, &tm_do, n, it0, n0, bh, sbase, a, ab);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    mma_role<D>(n, tmem, sbase, ab);
+  } else {
+    drain_role<D>(&tm_dq, n, it0, bh, tmem, sbase, ab);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Pre- and post-passes (memory-bound, plain loads and stores)
+// ------------------------------------------------------------------------------------------------
+// D/8 threads per padded query row: each reads 8 elements of O and dO, the group reduces
+// D_i = sum(dO_i * O_i); the group also zeroes the row of the dQ array.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       const float* __restrict__ lse, float* __restrict__ nl2,
+                                                       float* __restrict__ negd, float* __restrict__ dq_acc, int BH,
+                                                       int Nq, int Nq_pad) {
+  constexpr int G = D / 8;  // threads per row (8 or 16)
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long r = t / G;
+  const int g = static_cast<int>(t % G);
+  const bool live = r < static_cast<long long>(BH) * Nq_pad;
+  const long long bh = live ? r / Nq_pad : 0;
+  const int i = live ? static_cast<int>(r % Nq_pad) : 0;
+  float acc = 0.f;
+  const bool valid = live && i < Nq;
+  if (valid) {
+    const size_t off = (static_cast<size_t>(bh) * Nq + i) * D + 8 * g;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = fmaf(bf16lo_to_f32(av[k]), bf16lo_to_f32(bv[k]), acc);
+      acc = fmaf(bf16hi_to_f32(av[k]), bf16hi_to_f32(bv[k]), acc);
+    }
+  }
+#pragma unroll
+  for (int s = G / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (!live) return;
+  float4* z = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * Nq_pad + i) * D + 8 * g);
+  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (g == 0) {
+    const size_t ri = static_cast<size_t>(bh) * Nq_pad + i;
+    nl2[ri] = valid ? -lse[static_cast<size_t>(bh) * Nq + i] * kLog2e : -INFINITY;
+    negd[ri] = valid ? -acc : 0.f;
+  }
+}
+
+// dQ = scale * accumulated dQ, 8 elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                                                     int BH, int Nq, int Nq_pad, float scale) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(BH) * Nq * (D / 8);
+  if (t >= total) return;
+  const long long r = t / (D / 8);
+  const int g = static_cast<int>(t % (D / 8));
+  const long long bh = r / Nq;
+  const int i = static_cast<int>(r % Nq);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + (static_cast<size_t>(bh) * Nq_pad + i) * D + 8 * g);
+  const float4 x = src[0], y = src[1];
+  uint4 out;
+  out.x = pack_bf16x2(x.x * scale, x.y * scale);
+  out.y = pack_bf16x2(x.z * scale, x.w * scale);
+  out.z = pack_bf16x2(y.x * scale, y.y * scale);
+  out.w = pack_bf16x2(y.z * scale, y.w * scale);
+  *reinterpret_cast<uint4*>(dq + static_cast<size_t>(r) * D + 8 * g) = out;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, unsigned int* status,
+                         unsigned long long timeout_ns, cudaStream_t stream) {
+  using C = BCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int BH = p.B * p.H;
+  const int Nq_pad = bwd_padded_rows(p.Nq);
+  {
+    const long long threads = static_cast<long long>(BH) * Nq_pad * (D / 8);
+    const unsigned int grid = static_cast<unsigned int>((threads + 255) / 256);
+    bwd_prep_kernel<D><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(p.o),
+                                                  static_cast<const __nv_bfloat16*>(p.dout), p.lse, p.ws_nl2,
+                                                  p.ws_negd, p.ws_dq, BH, p.Nq, Nq_pad);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  BArgs a;
+  a.dk = static_cast<__nv_bfloat16*>(p.dk);
+  a.dv = static_cast<__nv_bfloat16*>(p.dv);
+  a.nl2 = p.ws_nl2;
+  a.negd = p.ws_negd;
+  a.BH = BH;
+  a.Nq = p.Nq;
+  a.Nk = p.Nk;
+  a.Nq_pad = Nq_pad;
+  a.NqT = Nq_pad / kBM;
+  a.causal = p.causal;
+  a.off = p.Nk - p.Nq;
+  a.c_log2 = p.scale * kLog2e;
+  a.scale = p.scale;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  const unsigned int grid = static_cast<unsigned int>((p.Nk + kBN - 1) / kBN) * static_cast<unsigned int>(BH);
+  bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    const long long threads = static_cast<long long>(BH) * p.Nq * (D / 8);
+    const unsigned int g2 = static_cast<unsigned int>((threads + 255) / 256);
+    bwd_dq_kernel<D><<<g2, 256, 0, stream>>>(p.ws_dq, static_cast<__nv_bfloat16*>(p.dq), BH, p.Nq, Nq_pad, p.scale);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, unsigned int* status,
+                            unsigned long long timeout_ns, cudaStream_t stream) {
+  if (p.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
+  return launch_bwd_d<128>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
+}
+
+}  // namespace fattn

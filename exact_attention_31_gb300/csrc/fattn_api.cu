@@ -93,6 +93,20 @@ bool make_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// [BH][rows][d] fp32 (the backward's dQ accumulator), 128-row x 32-column boxes, 128-byte swizzle.
+bool make_map_f32(CUtensorMap* map, void* base, int BH, int rows, int d) {
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool positive_sizes(long long a, long long b, long long c, long long d) {
   return a >= 1 && b >= 1 && c >= 1 && d >= 1;
 }
@@ -138,6 +152,51 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
   FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, test_drop_kv_block()};
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d) {
+  if (!positive_sizes(B, H, Nq, d)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * bwd_padded_rows(Nq);
+  return align_up(rows * d * sizeof(float), 256) + 2 * align_up(rows * sizeof(float), 256);
+}
+
+fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nq, Nk)) return FATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FATTN_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL / 256) return FATTN_ERR_INVALID_ARG;
+  if (Nq > 0x7fffffff - 128) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const size_t need = fattn_bwd_workspace_size(B, H, Nq, d);
+  if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+
+  const int BH = B * H;
+  const int Nq_pad = bwd_padded_rows(Nq);
+  const size_t rows = static_cast<size_t>(BH) * Nq_pad;
+  char* ws = static_cast<char*>(workspace);
+  float* ws_dq = reinterpret_cast<float*>(ws);
+  float* ws_nl2 = reinterpret_cast<float*>(ws + align_up(rows * d * sizeof(float), 256));
+  float* ws_negd = reinterpret_cast<float*>(ws + align_up(rows * d * sizeof(float), 256) +
+                                            align_up(rows * sizeof(float), 256));
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_map(&tq, q, BH, Nq, d) || !make_map(&tk, k, BH, Nk, d) || !make_map(&tv, v, BH, Nk, d) ||
+      !make_map(&tdo, dout, BH, Nq, d) || !make_map_f32(&tdq, ws_dq, BH, Nq_pad, d))
+    return FATTN_ERR_CUDA;
+  unsigned int* status = nullptr;
+  if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
+  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, causal, scale, ws_dq, ws_nl2, ws_negd};
+  if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
   return FATTN_OK;

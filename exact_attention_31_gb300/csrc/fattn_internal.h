@@ -39,6 +39,26 @@ struct DecodeProblem {
   float* ws_ml;      // [B*H*num_splits, 2] partial (m, l), m in log2 units of the scaled score
 };
 
+struct BwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, Nq, Nk, d, causal;
+  float scale;
+  float* ws_dq;    // [B*H][Nq_pad][d] fp32 dQ accumulator
+  float* ws_nl2;   // [B*H][Nq_pad] -L * log2(e)
+  float* ws_negd;  // [B*H][Nq_pad] -D
+};
+
+// Query rows of the backward workspace per head: Nq rounded up to the 128-row query tile.
+inline int bwd_padded_rows(int Nq) { return (Nq + 127) / 128 * 128; }
+
 // Keys per decode block: the unit a split is made of.
 constexpr int kDecodeBlockKeys = 64;
 
@@ -49,5 +69,11 @@ cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUt
                            cudaStream_t stream);
 
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+
+// Backward: q, k, v, dout as for the prefill; tdq describes ws_dq as a 3-D [B*H][Nq_pad][d] fp32
+// tensor with 32-element (128-byte) inner boxes of 128 rows and 128-byte swizzle.
+cudaError_t launch_backward(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, unsigned int* status,
+                            unsigned long long timeout_ns, cudaStream_t stream);
 
 }  // namespace fattn

@@ -12,6 +12,10 @@ The named workloads are the sizes the library is measured and checked on:
                                the query rows of every head multiplied by 8
   prefill_b1h32_n8192_d64      B=1,  H=32, Nq=Nk=8192,  d=64,  causal
   decode_b32h32_nk16384_d128   B=32, H=32, Nq=1, Nk=16384, d=128, no mask
+
+The backward pass is checked and measured on the prefill shapes; its upstream gradient dO is drawn
+by make_dout from a generator of its own (seed + DOUT_SEED_OFFSET), so Q, K and V stay those of the
+forward workload.
 """
 
 from __future__ import annotations
@@ -21,6 +25,7 @@ import dataclasses
 import torch
 
 SEED_BASE = 0xFA77E000
+DOUT_SEED_OFFSET = 0x100
 
 
 @dataclasses.dataclass(frozen=True)
@@ -107,3 +112,13 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int, device="cpu", 
 
 def make_workload(w: Workload, device="cpu"):
     return make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed, device, w.boost_frac, w.boost)
+
+
+def make_dout(B: int, H: int, Nq: int, d: int, seed: int, device="cpu"):
+    """Seeded bf16 upstream gradient dO [B,H,Nq,d], iid N(0, 1) rounded once to bf16, drawn from a
+    generator seeded with seed + DOUT_SEED_OFFSET."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) + DOUT_SEED_OFFSET)
+    chunk = 1 if B * H * Nq * d > (1 << 28) else None
+    return _randn_bf16((B, H, Nq, d), gen, device, chunk)

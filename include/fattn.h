@@ -1,5 +1,6 @@
 /*
- * fattn.h -- C ABI of libfattn: exact fused attention forward and split-KV decode for sm_103a.
+ * fattn.h -- C ABI of libfattn: exact fused attention forward, its backward, and split-KV decode
+ * for sm_103a.
  *
  * The operation is the one the pages define: O = softmax(scale * Q K^T + mask) V, computed tile by
  * tile with the online-softmax recurrence (running max m, running sum l, unnormalised O rescaled by
@@ -60,6 +61,38 @@ typedef enum fattn_status {
  */
 fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                        int Nq, int Nk, int d, int causal, float scale, void* stream);
+
+/*
+ * fattn_bwd -- gradients of the attention forward ("Flash Attention: The Hidden Gem", Phase 2:
+ * Chain Rule Through a Matrix Multiply, The Softmax Jacobian, The D Shortcut, The Algorithm).
+ *
+ * For O = softmax(scale * Q K^T + mask) V and an upstream gradient dO it writes
+ *   dV = P^T dO,   dQ = scale * dS K,   dK = scale * dS^T Q,
+ * where P = exp(scale * Q K^T - L) is recomputed from the forward's L, dP = dO V^T,
+ * D = rowsum(dO o O) and dS = P o (dP - D).  The pages state the gradients without the scale; the
+ * factor on dQ and dK is the chain rule through S = scale * Q K^T.
+ *
+ *   q, k, v  bf16, as given to fattn_fwd
+ *   o        bf16 [B, H, Nq, d]  the forward output for these q, k, v (only D = rowsum(dO o O) uses it)
+ *   lse      fp32 [B, H, Nq]     the forward's L (natural log), as fattn_fwd writes it
+ *   dout     bf16 [B, H, Nq, d]  upstream gradient dO
+ *   dq       bf16 [B, H, Nq, d]  written
+ *   dk, dv   bf16 [B, H, Nk, d]  written
+ *   B, H, Nq, Nk, d, causal, scale   as for fattn_fwd (the same mask must be used)
+ *   workspace        device memory of at least fattn_bwd_workspace_size(B, H, Nq, d) bytes,
+ *                    256-byte aligned, owned by the caller; its contents on entry do not matter
+ *                    and it holds the fp32 dQ accumulator, D and L * log2(e) on return
+ *
+ * Three kernels run in order on `stream`: a pre-pass (D per row, the accumulator cleared), the fused
+ * kernel (one CTA per 128-key tile of a head; dK and dV stay on chip, dQ is added into the fp32
+ * accumulator), and a pass that scales and rounds dQ.  Calls sharing a workspace must not overlap.
+ * Accumulation is fp32; P and dS are rounded to bf16 before the products that consume them, and
+ * dQ's accumulation order across key tiles is not fixed, so dQ is not bitwise reproducible.
+ */
+size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d);
+fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fattn_decode_num_splits -- the number of key splits fattn_decode uses for a request.

@@ -28,8 +28,9 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ("fattn_fwd", "fattn_decode", "fattn_decode_workspace_size", "fattn_status_string",
-                     "fattn_last_error", "fattn_decode_num_splits"):
+    for required in ("fattn_fwd", "fattn_bwd", "fattn_bwd_workspace_size", "fattn_decode",
+                     "fattn_decode_workspace_size", "fattn_status_string", "fattn_last_error",
+                     "fattn_decode_num_splits"):
         assert required in names
 
 
@@ -98,6 +99,49 @@ def test_decode_workspace_size(L):
 ])
 def test_decode_rejects_bad_arguments(L, args, expect):
     assert L.fattn_decode(*args, None) == expect
+
+
+def test_bwd_workspace_size(L):
+    # fp32 dQ accumulator [B*H][Nq_pad][d] plus -L*log2e and -D [B*H][Nq_pad], each padded to 256 B
+    def pad(x):
+        return (x + 255) // 256 * 256
+    assert L.fattn_bwd_workspace_size(1, 32, 8192, 64) == pad(32 * 8192 * 64 * 4) + 2 * pad(32 * 8192 * 4)
+    assert L.fattn_bwd_workspace_size(2, 3, 300, 128) == pad(6 * 384 * 128 * 4) + 2 * pad(6 * 384 * 4)
+    assert L.fattn_bwd_workspace_size(1, 1, 1, 64) == pad(128 * 64 * 4) + 2 * pad(128 * 4)
+    assert L.fattn_bwd_workspace_size(0, 1, 8, 64) == 0
+
+
+W = 1 << 24  # a large-enough workspace size for the rejections below
+BWD_OK = (A, A, A, A, A, A, A, A, A, 1, 1, 8, 8, 64, 0, 0.125, A, W)
+
+
+def _bwd(**changes):
+    names = ["q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv", "B", "H", "Nq", "Nk", "d", "causal", "scale",
+             "ws", "ws_bytes"]
+    args = list(BWD_OK)
+    for k, val in changes.items():
+        args[names.index(k)] = val
+    return tuple(args)
+
+
+@pytest.mark.parametrize("args,expect", [
+    (_bwd(q=None), 1),
+    (_bwd(lse=None), 1),
+    (_bwd(dout=None), 1),
+    (_bwd(dk=A + 2), 1),                  # misaligned output
+    (_bwd(lse=A + 2), 1),                 # misaligned lse
+    (_bwd(ws=None), 1),
+    (_bwd(ws=A + 16), 1),                 # workspace not 256-byte aligned
+    (_bwd(ws_bytes=1024), 1),             # workspace too small
+    (_bwd(Nq=0), 1),
+    (_bwd(causal=1, Nq=9), 1),            # causal with Nq > Nk
+    (_bwd(causal=3), 1),
+    (_bwd(scale=0.0), 1),
+    (_bwd(scale=float("nan")), 1),
+    (_bwd(d=96), 2),
+])
+def test_bwd_rejects_bad_arguments(L, args, expect):
+    assert L.fattn_bwd(*args, None) == expect
 
 
 def test_binding_fails_loudly_without_cuda_tensors():
