@@ -13,21 +13,24 @@
 // an fp32 array in device memory by every key tile that sees it.
 //
 // Three kernels run in stream order:
-//   bwd_prep_kernel  D_i (stored negated) and -L_i * log2(e) per query row into a padded workspace;
-//                    rows past Nq get (0, -inf) so that their P is exactly 0; zeroes the dQ array
+//   bwd_prep_kernel  per query row, -L_i / scale and -D_i, each split into three bf16 terms (see
+//                    below), into a padded workspace; rows past Nq get -inf and 0 so that their P is
+//                    exactly 0; zeroes the dQ array
 //   bwd_kernel       one CTA per (head, 128-key tile); walks the query tiles that can see its keys
 //   bwd_dq_kernel    dQ = scale * accumulated array, rounded to bf16
 //
 // bwd_kernel works on transposed tiles so that one thread owns one key: S^T = K Q^T and
 // dP^T = V dO^T land in tensor memory with keys on the 128 lanes and the 128 queries of the tile
-// along the columns.  Thread layout (448 threads):
+// along the columns.  Thread layout (480 threads):
 //   warps 0-7    compute: warp w reads lanes 32*(w%4).. and the query half w/4 of S^T and dP^T,
 //                forms P^T = exp2(S^T * scale*log2e - L*log2e) and dS^T = P^T o (dP^T - D), writes
 //                P^T (bf16) back into tensor memory and dS^T (bf16) into shared memory
 //   warp  8      TMA producer: K_j and V_j once, then Q_i, dO_i, -L_i*log2e, -D_i per query tile
-//   warp  9      MMA issuer and tensor-memory owner
+//   warp  9      MMA issuer (dP^T, dV, dK, dQ; with d = 128 also S^T) and tensor-memory owner
 //   warps 10-13  dQ drain: one thread per query row reads dQ_i from tensor memory, stages it in
 //                shared memory and adds it into the fp32 array with a TMA reduce
+//   warp  14     (d = 64) issues S^T = K Q_i^T for every tile as soon as its buffer is free, so the
+//                main MMA warp never waits for the dQ drain
 // The five products per query tile are tcgen05.mma with M = 128:
 //   S^T  = K Q^T        A = K (K-major)          B = Q (K-major)
 //   dP^T = V dO^T       A = V (K-major)          B = dO (K-major)
@@ -35,6 +38,14 @@
 //   dK  += dS^T Q       A = dS^T (K-major)       B = Q read MN-major
 //   dQ   = dS K         A = dS^T read MN-major   B = K read MN-major
 // so one shared-memory copy of dS^T serves both of its products.
+//
+// The per-query terms enter through the tensor core, not through shared-memory loads in the compute
+// warps: S^T and dP^T get one more K step of 16 columns whose A side is a constant block of ones and
+// whose B side holds, per query, the three bf16 terms of -L_i / scale (for S) or -D_i (for dP), each
+// halved and written into both 8-column halves of the step.  The products come out as
+// S'^T = S^T - L / scale and dP'^T = dP^T - D, so the compute warps form P^T = exp2(S'^T * scale *
+// log2(e)) and dS^T = P^T o dP'^T with one multiply each.  Three bf16 terms carry an fp32 value to
+// within 2^-24 of its magnitude; halving is exact.
 //
 // Tensor memory (512 columns):
 //   d = 64:  S^T buffers at 0 and 128 (two query tiles in flight), dP^T at 256, dV at 384, dK at
@@ -54,10 +65,11 @@ namespace {
 
 constexpr int kBM = 128;  // queries per inner step (columns of S^T)
 constexpr int kBN = 128;  // keys per CTA (TMEM lanes)
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDrainWarp0 = 10;
+constexpr int kSWarp = 14;  // issues the S^T products (d = 64)
 constexpr int kDrainBarrier = 1;  // named barrier id of the four drain warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes: one swizzled 64-column chunk of a tile
@@ -78,21 +90,28 @@ struct BCfg {
   static constexpr uint32_t kDSOff = kStageOff + kStages * 2 * kTile;
   static constexpr uint32_t kDQOff = kDSOff + kDSBufs * kDSBytes;  // 64 columns of dQ at a time
   static constexpr uint32_t kDQBytes = kBM * 64 * 4;
-  static constexpr uint32_t kLDOff = kDQOff + kDQBytes;  // stage s: -L*log2e [128], -D [128]
-  static constexpr uint32_t kBarOff = kLDOff + kStages * 1024;
+  static constexpr uint32_t kOnesOff = kDQOff + kDQBytes;  // [128 rows][16] bf16 of the constant A block
+  static constexpr uint32_t kExtBytes = kBM * 32;             // [128 rows][16] bf16
+  static constexpr uint32_t kExtOff = kOnesOff + kExtBytes;   // stage s: Q terms at + 2*s*kExtBytes, dO terms after
+  static constexpr uint32_t kBarOff = kExtOff + kStages * 2 * kExtBytes;
   // barrier indices
+  static_assert(kStages <= 4, "barrier slots");
   static constexpr int kKVFull = 0;
-  static constexpr int kQFull = 1;    // [2] Q_i, dO_i, -L, -D of a stage landed
-  static constexpr int kQEmpty = 3;   // [2] the stage's last reader (dK_i) done
-  static constexpr int kSFull = 5;    // [2] S^T of a buffer computed
-  static constexpr int kDPFull = 7;   // dP^T computed
-  static constexpr int kCDone = 8;    // compute warps done with a tile (one arrival per warp)
-  static constexpr int kDSEmpty = 9;  // [2] dK_i and dQ_i have read a dS^T buffer
-  static constexpr int kDQFull = 11;  // [2] dQ_i in tensor memory
-  static constexpr int kDQFree = 13;  // [2] dQ_i read out of tensor memory (one arrival per drain warp)
-  static constexpr int kAccDone = 15; // every MMA of the CTA done: dK, dV final
-  static constexpr int kDrain = 16;
-  static constexpr int kNumBars = 17;
+  static constexpr int kQFull = 1;     // [kStages] Q_i and its extra K-step block landed
+  static constexpr int kOFull = 5;     // [kStages] dO_i and its extra K-step block landed
+  static constexpr int kQEmpty = 9;    // [kStages] Q_i's last reader (dK_i) done
+  static constexpr int kOEmpty = 13;   // [kStages] dO_i's last reader (dV_i) done
+  static constexpr int kSFull = 17;    // [2] S^T of a buffer computed
+  static constexpr int kDPFull = 19;   // dP^T computed
+  static constexpr int kCDone = 20;    // compute warps done with a tile (one arrival per warp)
+  static constexpr int kDSEmpty = 21;  // [2] dK_i and dQ_i have read a dS^T buffer
+  static constexpr int kDQFull = 23;   // [2] dQ_i in tensor memory
+  static constexpr int kDQFree = 25;   // [2] dQ_i read out of tensor memory (one arrival per drain warp)
+  static constexpr int kAccDone = 27;  // every MMA of the CTA done: dK, dV final
+  static constexpr int kDrain = 28;
+  static constexpr int kDPFree = 29;   // compute warps have read dP^T (one arrival per warp)
+  static constexpr int kDrainS = 30;
+  static constexpr int kNumBars = 31;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -115,8 +134,8 @@ __host__ __device__ constexpr uint32_t p_step_col(int kk) { return kk < 4 ? 8u *
 struct BArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float* nl2;   // [BH][Nq_pad]  -L * log2(e)
-  const float* negd;  // [BH][Nq_pad]  -D
+  const __nv_bfloat16* ext_q;   // [BH][Nq_pad][16]  terms of -L / scale
+  const __nv_bfloat16* ext_do;  // [BH][Nq_pad][16]  terms of -D
   int BH, Nq, Nk, Nq_pad, NqT, causal, off;
   float c_log2;  // scale * log2(e)
   float scale;
@@ -157,22 +176,13 @@ __device__ __forceinline__ void wait_dep(uint32_t (&r)[32]) {
         "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
 }
 
-// (o0, o1) = (a0, a1) * b + (c0, c1)
-__device__ __forceinline__ void ffma2(float& o0, float& o1, float a0, float a1, float b, float c0, float c1) {
-  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
-      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %6};\n\t"
-      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+// (o0, o1) = (a0, a1) * (b0, b1)
+__device__ __forceinline__ void fmul2(float& o0, float& o1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
       : "=f"(o0), "=f"(o1)
-      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
-}
-// (o0, o1) = (a0, a1) * ((b0, b1) + (c0, c1))
-__device__ __forceinline__ void fmul_add2(float& o0, float& o1, float a0, float a1, float b0, float b1,
-                                          float c0, float c1) {
-  asm("{\n\t.reg .b64 x, y, z, t, w;\n\t"
-      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
-      "add.rn.f32x2 t, y, z;\n\tmul.rn.f32x2 w, x, t;\n\tmov.b64 {%0, %1}, w;\n\t}"
-      : "=f"(o0), "=f"(o1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -197,7 +207,6 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
   bool ok = true;
   for (int i = 0; i < n; ++i) {
     const int b = i % C::kSBufs;
-    const int st = i % C::kStages;
     const int dsb = i % C::kDSBufs;
     if (!warp_wait(sbar + 8 * (C::kSFull + b), (i / C::kSBufs) & 1, ab) ||
         !warp_wait(sbar + 8 * C::kDPFull, i & 1, ab) ||
@@ -209,8 +218,6 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
     const int q0 = (it0 + i) * kBM;
     const uint32_t tS = tmem + lane_field + C::col_s(b);
     const uint32_t tDP = tmem + lane_field + C::kColDP;
-    const float* nl2 = reinterpret_cast<const float*>(smem + C::kLDOff + st * 1024);
-    const float* negd = nl2 + kBM;
     const uint32_t ds_row = sbase + C::kDSOff + dsb * C::kDSBytes + half * kAtom + kr * 128;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
@@ -221,33 +228,32 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
       tmem_ld_32x32b_x32(tDP + qa, dp);
       wait_dep(s);
       wait_dep(dp);
+      if (C::kTwoS && cc == 1) {
+        // dP^T is in registers: the next tile's dP^T may be computed into the same columns.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbar + 8 * C::kDPFree);
+      }
+      // s = S'^T = S^T - L / scale and dp = dP'^T = dP^T - D for queries [q0 + qa, q0 + qa + 32).
       // Causal: key kidx is visible to query q iff kidx <= q + off.  Elements e < fv of this chunk
       // are masked.
       const int fv = a.causal ? kidx - a.off - (q0 + qa) : -1;
       const bool mask = __any_sync(0xffffffffu, fv > 0);
       uint32_t pp[16], pd[16];
 #pragma unroll
-      for (int k4 = 0; k4 < 8; ++k4) {
-        const float4 nl = *reinterpret_cast<const float4*>(nl2 + qa + 4 * k4);
-        const float4 nd = *reinterpret_cast<const float4*>(negd + qa + 4 * k4);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int e = 4 * k4 + 2 * hh;
-          float x0, x1;
-          ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), c, hh ? nl.z : nl.x,
-                hh ? nl.w : nl.y);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (mask) {
-            p0 = (e < fv) ? 0.f : p0;
-            p1 = (e + 1 < fv) ? 0.f : p1;
-          }
-          float d0, d1;
-          fmul_add2(d0, d1, p0, p1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), hh ? nd.z : nd.x,
-                    hh ? nd.w : nd.y);
-          pp[e >> 1] = pack_bf16x2(p0, p1);
-          pd[e >> 1] = pack_bf16x2(d0, d1);
+      for (int e = 0; e < 32; e += 2) {
+        float x0, x1;
+        fmul2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), c, c);
+        float p0 = ex2_approx(x0);
+        float p1 = ex2_approx(x1);
+        if (mask) {
+          p0 = (e < fv) ? 0.f : p0;
+          p1 = (e + 1 < fv) ? 0.f : p1;
         }
+        float d0, d1;
+        fmul2(d0, d1, p0, p1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]));
+        pp[e >> 1] = pack_bf16x2(p0, p1);
+        pd[e >> 1] = pack_bf16x2(d0, d1);
       }
       tmem_st_32x32b_x16(tS + p_col(half, ch), pp);
       // dS^T row kr, queries [qa, qa + 32): 16-byte units 4*ch .. 4*ch + 3 of this half's 128-byte
@@ -312,35 +318,39 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
     tma_load_3d(sbase + C::kKOff + ch * kAtom, tk, sbar + 8 * C::kKVFull, 64 * ch, n0, bh);
     tma_load_3d(sbase + C::kVOff + ch * kAtom, tv, sbar + 8 * C::kKVFull, 64 * ch, n0, bh);
   }
+  // Q_i (with its -L / scale terms) and dO_i (with its -D terms) are loaded separately: Q_i's stage
+  // is free once dK_i has read it, dO_i's once dV_i has.
   int issued = 0;
   bool ok = true;
-  for (int i = 0; i < n; ++i) {
+  for (int i = 0; i < n && ok; ++i) {
     const int st = i % C::kStages, use = i / C::kStages;
-    if (use > 0 && !thread_wait(sbar + 8 * (C::kQEmpty + st), (use - 1) & 1, ab)) {
-      ok = false;
-      break;
-    }
     const int q0 = (it0 + i) * kBM;
-    const uint32_t bar = sbar + 8 * (C::kQFull + st);
-    const uint32_t dst = sbase + C::kStageOff + st * 2 * C::kTile;
-    mbar_arrive_expect_tx(bar, 2 * C::kTile + 2 * kBM * 4);
+    const size_t r0 = (static_cast<size_t>(bh) * a.Nq_pad + q0) * 16;
 #pragma unroll
-    for (int ch = 0; ch < C::kChunks; ++ch) {
-      tma_load_3d(dst + ch * kAtom, tq, bar, 64 * ch, q0, bh);
-      tma_load_3d(dst + C::kTile + ch * kAtom, tdo, bar, 64 * ch, q0, bh);
+    for (int w = 0; w < 2; ++w) {
+      if (use > 0 && !thread_wait(sbar + 8 * ((w ? C::kOEmpty : C::kQEmpty) + st), (use - 1) & 1, ab)) {
+        ok = false;
+        break;
+      }
+      const uint32_t bar = sbar + 8 * ((w ? C::kOFull : C::kQFull) + st);
+      const uint32_t dst = sbase + C::kStageOff + (2 * st + w) * C::kTile;
+      mbar_arrive_expect_tx(bar, C::kTile + C::kExtBytes);
+#pragma unroll
+      for (int ch = 0; ch < C::kChunks; ++ch) tma_load_3d(dst + ch * kAtom, w ? tdo : tq, bar, 64 * ch, q0, bh);
+      bulk_load(sbase + C::kExtOff + (2 * st + w) * C::kExtBytes, (w ? a.ext_do : a.ext_q) + r0, C::kExtBytes, bar);
+      issued = 2 * i + w + 1;
     }
-    const size_t r0 = static_cast<size_t>(bh) * a.Nq_pad + q0;
-    bulk_load(sbase + C::kLDOff + st * 1024, a.nl2 + r0, kBM * 4, bar);
-    bulk_load(sbase + C::kLDOff + st * 1024 + kBM * 4, a.negd + r0, kBM * 4, bar);
-    issued = i + 1;
   }
   if (!ok) {
     // Let the copies already in flight land before the CTA's shared memory goes away.
     const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
     volatile uint32_t never = 0;
     mbar_wait_bounded(sbar + 8 * C::kKVFull, 0, &never, until);
-    for (int i = max(0, issued - C::kStages); i < issued; ++i)
-      mbar_wait_bounded(sbar + 8 * (C::kQFull + i % C::kStages), (i / C::kStages) & 1, &never, until);
+    for (int idx = max(0, issued - 2 * C::kStages); idx < issued; ++idx) {
+      const int i = idx >> 1, w = idx & 1;
+      mbar_wait_bounded(sbar + 8 * ((w ? C::kOFull : C::kQFull) + i % C::kStages), (i / C::kStages) & 1, &never,
+                        until);
+    }
   }
 }
 
@@ -355,6 +365,7 @@ struct BMma {
   uint64_t q_kmaj0, do_kmaj0;      // stage 0 Q_i, dO_i as K-major operands
   uint64_t q_mn0, do_mn0;          // ... and as MN-major operands
   uint64_t ds_kmaj0, ds_mn0;       // dS^T buffer 0, K-major (for dK) and MN-major (for dQ)
+  uint64_t ones, ext_q0, ext_do0;  // the extra K step: constant A block, stage 0 B blocks
   uint32_t lead;
 
   __device__ __forceinline__ void init(uint32_t tmem_, uint32_t sbase) {
@@ -369,6 +380,9 @@ struct BMma {
     do_mn0 = smem_desc_sw128(sbase + C::kStageOff + C::kTile, kAtom, 1024);
     ds_kmaj0 = smem_desc_sw128(sbase + C::kDSOff, 16, 1024);
     ds_mn0 = smem_desc_sw128(sbase + C::kDSOff, kAtom, 1024);
+    ones = smem_desc_sw32(sbase + C::kOnesOff);
+    ext_q0 = smem_desc_sw32(sbase + C::kExtOff);
+    ext_do0 = smem_desc_sw32(sbase + C::kExtOff + C::kExtBytes);
     lead = elect_lane();
   }
   // start-address advances, in 16-byte units
@@ -379,19 +393,24 @@ struct BMma {
   // MN-major operand, K step kk of 16 rows
   __host__ __device__ static constexpr uint64_t mn_adv(int kk) { return static_cast<uint64_t>(kk * 16 * 128) >> 4; }
 
+  __host__ __device__ static constexpr uint64_t ext_adv(int st) { return static_cast<uint64_t>(st) * (2 * C::kExtBytes >> 4); }
+  // S'^T = K Q^T + ones (terms of -L / scale)^T
   __device__ __forceinline__ void issue_s(int b, int st) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM, false);
     const uint64_t bq = q_kmaj0 + stage_adv(st);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_lead(tmem + C::col_s(b), k_kmaj + kmaj_adv(kk), bq + kmaj_adv(kk), id, kk > 0 ? 1u : 0u, lead);
+    mma_ss_lead(tmem + C::col_s(b), ones, ext_q0 + ext_adv(st), id, 1u, lead);
   }
+  // dP'^T = V dO^T + ones (terms of -D)^T
   __device__ __forceinline__ void issue_dp(int st) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM, false);
     const uint64_t bd = do_kmaj0 + stage_adv(st);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_lead(tmem + C::kColDP, v_kmaj + kmaj_adv(kk), bd + kmaj_adv(kk), id, kk > 0 ? 1u : 0u, lead);
+    mma_ss_lead(tmem + C::kColDP, ones, ext_do0 + ext_adv(st), id, 1u, lead);
   }
   __device__ __forceinline__ void issue_dv(int b, int st, bool first) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, D, true);
@@ -421,64 +440,95 @@ struct BMma {
   }
 };
 
+// d = 64, main MMA warp: dP^T of the next tile as soon as the compute warps have read this tile's,
+// then this tile's dV, dK and dQ once its P^T and dS^T are written.  S^T is the other warp's.
 template <int D>
-__device__ __forceinline__ bool mma_schedule(int n, const BMma<D>& m, const Abort& ab) {
+__device__ __forceinline__ bool mma_schedule_two(int n, const BMma<D>& m, const Abort& ab) {
   using C = BCfg<D>;
-  if (!m.wait(C::kKVFull, 0, ab) || !m.wait(C::kQFull, 0, ab)) return false;
+  if (!m.wait(C::kKVFull, 0, ab) || !m.wait(C::kOFull, 0, ab)) return false;
+  tc_fence_after();
+  m.issue_dp(0);
+  m.commit(C::kDPFull);
+  for (int i = 0; i < n; ++i) {
+    const int b = i & 1, st = i % C::kStages, dsb = i % C::kDSBufs;
+    if (i + 1 < n) {
+      if (!m.wait(C::kDPFree, i, ab) || !m.wait(C::kOFull + (i + 1) % C::kStages, (i + 1) / C::kStages, ab))
+        return false;
+      tc_fence_after();
+      m.issue_dp((i + 1) % C::kStages);
+      m.commit(C::kDPFull);
+    }
+    if (!m.wait(C::kCDone, i, ab)) return false;
+    tc_fence_after();
+    // dQ_i first: the drain warps can then empty its columns, which S^T of tile i+2 reuses, while dK_i
+    // and dV_i run.
+    m.issue_dq(b, dsb);
+    m.commit(C::kDQFull + b);
+    m.issue_dk(dsb, st, i == 0);
+    m.commit(C::kDSEmpty + dsb);
+    m.commit(C::kQEmpty + st);
+    m.issue_dv(b, st, i == 0);
+    m.commit(C::kOEmpty + st);
+  }
+  m.commit(C::kAccDone);
+  return true;
+}
+
+// d = 64, S^T warp: S^T of tile t into buffer t % 2 once tile t-2 is done with it -- dV_{t-2} has read
+// P^T_{t-2} (the dO stage of tile t-2 is released after dV_{t-2}) and the drain warps have read dQ_{t-2}
+// -- and Q_t has landed.
+template <int D>
+__device__ __forceinline__ bool mma_schedule_s(int n, const BMma<D>& m, const Abort& ab) {
+  using C = BCfg<D>;
+  if (!m.wait(C::kKVFull, 0, ab)) return false;
+  for (int t = 0; t < n; ++t) {
+    const int b = t & 1;
+    if (t >= 2) {
+      const int u = t - 2;
+      if (!m.wait(C::kDQFree + b, u / 2, ab) || !m.wait(C::kOEmpty + u % C::kStages, u / C::kStages, ab))
+        return false;
+    }
+    if (!m.wait(C::kQFull + t % C::kStages, t / C::kStages, ab)) return false;
+    tc_fence_after();
+    m.issue_s(b, t % C::kStages);
+    m.commit(C::kSFull + b);
+  }
+  return true;
+}
+
+// d = 128, one MMA warp: one S^T buffer, dQ in the dP^T columns.
+template <int D>
+__device__ __forceinline__ bool mma_schedule_one(int n, const BMma<D>& m, const Abort& ab) {
+  using C = BCfg<D>;
+  if (!m.wait(C::kKVFull, 0, ab) || !m.wait(C::kQFull, 0, ab) || !m.wait(C::kOFull, 0, ab)) return false;
   tc_fence_after();
   m.issue_s(0, 0);
   m.commit(C::kSFull);
   m.issue_dp(0);
   m.commit(C::kDPFull);
-  if (C::kTwoS && n > 1) {
-    if (!m.wait(C::kQFull + 1, 0, ab)) return false;
-    tc_fence_after();
-    m.issue_s(1, 1);
-    m.commit(C::kSFull + 1);
-  }
   for (int i = 0; i < n; ++i) {
-    const int b = i % C::kSBufs, st = i % C::kStages, dsb = i % C::kDSBufs;
+    const int dsb = i % C::kDSBufs;
     if (!m.wait(C::kCDone, i, ab)) return false;
     tc_fence_after();
-    if constexpr (C::kTwoS) {
-      // dP^T of the next tile first (its dO stage was waited for when its S^T was issued), so its
-      // compute can start while this tile's gradients are accumulated.
-      if (i + 1 < n) {
-        m.issue_dp((i + 1) % C::kStages);
-        m.commit(C::kDPFull);
-      }
-      m.issue_dv(b, st, i == 0);
-      m.issue_dk(dsb, st, i == 0);
-      m.commit(C::kQEmpty + st);
-      m.issue_dq(b, dsb);
-      m.commit(C::kDQFull + b);
-      m.commit(C::kDSEmpty + dsb);
-      if (i + 2 < n) {
-        // S^T of tile i+2 reuses this buffer: after dV_i has read P^T (issue order) and after the
-        // drain warps have read dQ_i out of it.
-        if (!m.wait(C::kDQFree + b, i / 2, ab) || !m.wait(C::kQFull + (i + 2) % C::kStages, (i + 2) / C::kStages, ab))
-          return false;
-        tc_fence_after();
-        m.issue_s(b, (i + 2) % C::kStages);
-        m.commit(C::kSFull + b);
-      }
-    } else {
-      m.issue_dv(0, 0, i == 0);
-      m.issue_dk(dsb, 0, i == 0);
-      m.commit(C::kQEmpty);
-      m.issue_dq(0, dsb);  // into the dP^T columns, read by the compute warps already
-      m.commit(C::kDQFull);
-      m.commit(C::kDSEmpty + dsb);
-      if (i + 1 < n) {
-        if (!m.wait(C::kQFull, i + 1, ab)) return false;
-        tc_fence_after();
-        m.issue_s(0, 0);
-        m.commit(C::kSFull);
-        if (!m.wait(C::kDQFree, i, ab)) return false;
-        tc_fence_after();
-        m.issue_dp(0);
-        m.commit(C::kDPFull);
-      }
+    // dV_i, dK_i, then dQ_i: with one S^T buffer the next S^T waits for dV_i anyway, and dO_{i+1} and
+    // Q_{i+1} can start loading as early as possible.
+    m.issue_dv(0, 0, i == 0);
+    m.commit(C::kOEmpty);
+    m.issue_dk(dsb, 0, i == 0);
+    m.commit(C::kQEmpty);
+    m.issue_dq(0, dsb);  // into the dP^T columns, read by the compute warps already
+    m.commit(C::kDQFull);
+    m.commit(C::kDSEmpty + dsb);
+    if (i + 1 < n) {
+      // S^T of the next tile after dV_i has read P^T from the same columns (issue order).
+      if (!m.wait(C::kQFull, i + 1, ab)) return false;
+      tc_fence_after();
+      m.issue_s(0, 0);
+      m.commit(C::kSFull);
+      if (!m.wait(C::kDQFree, i, ab) || !m.wait(C::kOFull, i + 1, ab)) return false;
+      tc_fence_after();
+      m.issue_dp(0);
+      m.commit(C::kDPFull);
     }
   }
   m.commit(C::kAccDone);
@@ -486,16 +536,19 @@ __device__ __forceinline__ bool mma_schedule(int n, const BMma<D>& m, const Abor
 }
 
 template <int D>
-__device__ __forceinline__ void mma_role(int n, uint32_t tmem, uint32_t sbase, const Abort& ab) {
+__device__ __forceinline__ void mma_role(int n, uint32_t tmem, uint32_t sbase, bool s_warp, const Abort& ab) {
   using C = BCfg<D>;
   BMma<D> m;
   m.init(tmem, sbase);
-  const bool ok = mma_schedule<D>(n, m, ab);
+  bool ok;
+  if constexpr (C::kTwoS) ok = s_warp ? mma_schedule_s<D>(n, m, ab) : mma_schedule_two<D>(n, m, ab);
+  else ok = mma_schedule_one<D>(n, m, ab);
   // Every MMA (and every arrival its commits make) completes before the CTA winds down.
-  m.commit(C::kDrain);
+  const int drain = s_warp ? C::kDrainS : C::kDrain;
+  m.commit(drain);
   volatile uint32_t never = 0;
   const uint64_t until = ok ? ab.deadline : globaltimer_ns() + 50ull * 1000 * 1000;
-  mbar_wait_bounded(m.sbar + 8 * C::kDrain, 0, &never, until);
+  mbar_wait_bounded(m.sbar + 8 * drain, 0, &never, until);
   __syncwarp();
 }
 
@@ -584,9 +637,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(sbar + 8 * C::kKVFull, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(sbar + 8 * (C::kQFull + s), 1);
+      mbar_init(sbar + 8 * (C::kOFull + s), 1);
       mbar_init(sbar + 8 * (C::kQEmpty + s), 1);
+      mbar_init(sbar + 8 * (C::kOEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(sbar + 8 * (C::kSFull + s), 1);
       mbar_init(sbar + 8 * (C::kDSEmpty + s), 1);
       mbar_init(sbar + 8 * (C::kDQFull + s), 1);
@@ -596,12 +653,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sbar + 8 * C::kCDone, 8);  // one arrival per compute warp
     mbar_init(sbar + 8 * C::kAccDone, 1);
     mbar_init(sbar + 8 * C::kDrain, 1);
+    mbar_init(sbar + 8 * C::kDPFree, 8);  // one arrival per compute warp
+    mbar_init(sbar + 8 * C::kDrainS, 1);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
+  }
+  if (threadIdx.x < 2 * kBN) {
+    // The constant A block of the extra K step: every 16-byte half of every row is (1, 1, 1, 0, ..., 0)
+    // in bf16, so its layout does not depend on the swizzle pattern.
+    st_shared_v4(sbase + C::kOnesOff + 16 * threadIdx.x, 0x3F803F80u, 0x00003F80u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -615,7 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, &tm_do, n, it0, n0, bh, sbase, a, ab);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    mma_role<D>(n, tmem, sbase, ab);
+    mma_role<D>(n, tmem, sbase, false, ab);
+  } else if (warp == kSWarp) {
+    if (C::kTwoS) mma_role<D>(n, tmem, sbase, true, ab);
   } else {
     drain_role<D>(&tm_dq, n, it0, bh, tmem, sbase, ab);
   }
@@ -633,12 +700,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------------------
 // D/8 threads per padded query row: each reads 8 elements of O and dO, the group reduces
 // D_i = sum(dO_i * O_i); the group also zeroes the row of the dQ array.
+// One 32-byte row of the extra K step's B block: the value y as three bf16 terms t0 + t1 + t2 (each
+// the rounding of what the previous ones left), halved, in columns 0-2 and again in columns 8-10.
+// y = -inf gives (-inf, 0, 0).
+__device__ __forceinline__ void write_terms(__nv_bfloat16* row, float y) {
+  float t[3] = {y, 0.f, 0.f};
+  if (isfinite(y)) {
+    float r = y;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      t[j] = __bfloat162float(__float2bfloat16_rn(r));
+      r -= t[j];
+    }
+  }
+  const uint32_t w0 = pack_bf16x2(0.5f * t[0], 0.5f * t[1]);
+  const uint32_t w1 = pack_bf16x2(0.5f * t[2], 0.f);
+  uint4* dst = reinterpret_cast<uint4*>(row);
+  dst[0] = make_uint4(w0, w1, 0u, 0u);
+  dst[1] = make_uint4(w0, w1, 0u, 0u);
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
-                                                       const float* __restrict__ lse, float* __restrict__ nl2,
-                                                       float* __restrict__ negd, float* __restrict__ dq_acc, int BH,
-                                                       int Nq, int Nq_pad) {
+                                                       const float* __restrict__ lse, __nv_bfloat16* __restrict__ ext_q,
+                                                       __nv_bfloat16* __restrict__ ext_do, float* __restrict__ dq_acc,
+                                                       int BH, int Nq, int Nq_pad, float inv_scale) {
   constexpr int G = D / 8;  // threads per row (8 or 16)
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long r = t / G;
@@ -666,9 +753,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
   z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (g == 0) {
-    const size_t ri = static_cast<size_t>(bh) * Nq_pad + i;
-    nl2[ri] = valid ? -lse[static_cast<size_t>(bh) * Nq + i] * kLog2e : -INFINITY;
-    negd[ri] = valid ? -acc : 0.f;
+    const size_t ri = (static_cast<size_t>(bh) * Nq_pad + i) * 16;
+    write_terms(ext_q + ri, valid ? -lse[static_cast<size_t>(bh) * Nq + i] * inv_scale : -INFINITY);
+    write_terms(ext_do + ri, valid ? -acc : 0.f);
   }
 }
 
@@ -714,16 +801,18 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
     const long long threads = static_cast<long long>(BH) * Nq_pad * (D / 8);
     const unsigned int grid = static_cast<unsigned int>((threads + 255) / 256);
     bwd_prep_kernel<D><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(p.o),
-                                                  static_cast<const __nv_bfloat16*>(p.dout), p.lse, p.ws_nl2,
-                                                  p.ws_negd, p.ws_dq, BH, p.Nq, Nq_pad);
+                                                  static_cast<const __nv_bfloat16*>(p.dout), p.lse,
+                                                  static_cast<__nv_bfloat16*>(p.ws_ext_q),
+                                                  static_cast<__nv_bfloat16*>(p.ws_ext_do), p.ws_dq, BH, p.Nq,
+                                                  Nq_pad, 1.f / p.scale);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   BArgs a;
   a.dk = static_cast<__nv_bfloat16*>(p.dk);
   a.dv = static_cast<__nv_bfloat16*>(p.dv);
-  a.nl2 = p.ws_nl2;
-  a.negd = p.ws_negd;
+  a.ext_q = static_cast<const __nv_bfloat16*>(p.ws_ext_q);
+  a.ext_do = static_cast<const __nv_bfloat16*>(p.ws_ext_do);
   a.BH = BH;
   a.Nq = p.Nq;
   a.Nk = p.Nk;

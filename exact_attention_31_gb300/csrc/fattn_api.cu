@@ -160,7 +160,7 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
 size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d) {
   if (!positive_sizes(B, H, Nq, d)) return 0;
   const size_t rows = static_cast<size_t>(B) * H * bwd_padded_rows(Nq);
-  return align_up(rows * d * sizeof(float), 256) + 2 * align_up(rows * sizeof(float), 256);
+  return align_up(rows * d * sizeof(float), 256) + 2 * align_up(rows * 32, 256);
 }
 
 fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -186,16 +186,15 @@ fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* 
   const size_t rows = static_cast<size_t>(BH) * Nq_pad;
   char* ws = static_cast<char*>(workspace);
   float* ws_dq = reinterpret_cast<float*>(ws);
-  float* ws_nl2 = reinterpret_cast<float*>(ws + align_up(rows * d * sizeof(float), 256));
-  float* ws_negd = reinterpret_cast<float*>(ws + align_up(rows * d * sizeof(float), 256) +
-                                            align_up(rows * sizeof(float), 256));
+  void* ws_ext_q = ws + align_up(rows * d * sizeof(float), 256);
+  void* ws_ext_do = ws + align_up(rows * d * sizeof(float), 256) + align_up(rows * 32, 256);
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_map(&tq, q, BH, Nq, d) || !make_map(&tk, k, BH, Nk, d) || !make_map(&tv, v, BH, Nk, d) ||
       !make_map(&tdo, dout, BH, Nq, d) || !make_map_f32(&tdq, ws_dq, BH, Nq_pad, d))
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
-  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, causal, scale, ws_dq, ws_nl2, ws_negd};
+  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, causal, scale, ws_dq, ws_ext_q, ws_ext_do};
   if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;

@@ -52,8 +52,8 @@ struct BwdProblem {
   int B, H, Nq, Nk, d, causal;
   float scale;
   float* ws_dq;    // [B*H][Nq_pad][d] fp32 dQ accumulator
-  float* ws_nl2;   // [B*H][Nq_pad] -L * log2(e)
-  float* ws_negd;  // [B*H][Nq_pad] -D
+  void* ws_ext_q;   // [B*H][Nq_pad][16] bf16: three terms of -L / scale (per query row)
+  void* ws_ext_do;  // [B*H][Nq_pad][16] bf16: three terms of -D
 };
 
 // Query rows of the backward workspace per head: Nq rounded up to the 128-row query tile.

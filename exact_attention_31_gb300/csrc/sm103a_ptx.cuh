@@ -226,6 +226,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
   return d;
 }
 
+// Descriptor for a K-major operand with 32-byte swizzle: rows of 32 bytes (16 bf16, one K step),
+// 8-row atoms of 256 bytes stacked along M/N.
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;    // leading byte offset (unused within one K step)
+  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= 1ull << 46;
+  d |= 6ull << 61;  // 32-byte swizzle
+  return d;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {

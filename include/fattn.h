@@ -81,7 +81,7 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
  *   B, H, Nq, Nk, d, causal, scale   as for fattn_fwd (the same mask must be used)
  *   workspace        device memory of at least fattn_bwd_workspace_size(B, H, Nq, d) bytes,
  *                    256-byte aligned, owned by the caller; its contents on entry do not matter
- *                    and it holds the fp32 dQ accumulator, D and L * log2(e) on return
+ *                    and it holds the fp32 dQ accumulator and the per-row terms of D and L on return
  *
  * Three kernels run in order on `stream`: a pre-pass (D per row, the accumulator cleared), the fused
  * kernel (one CTA per 128-key tile of a head; dK and dV stay on chip, dQ is added into the fp32

@@ -102,12 +102,12 @@ def test_decode_rejects_bad_arguments(L, args, expect):
 
 
 def test_bwd_workspace_size(L):
-    # fp32 dQ accumulator [B*H][Nq_pad][d] plus -L*log2e and -D [B*H][Nq_pad], each padded to 256 B
+    # fp32 dQ accumulator [B*H][Nq_pad][d] plus two [B*H][Nq_pad][16] bf16 term blocks, each padded to 256 B
     def pad(x):
         return (x + 255) // 256 * 256
-    assert L.fattn_bwd_workspace_size(1, 32, 8192, 64) == pad(32 * 8192 * 64 * 4) + 2 * pad(32 * 8192 * 4)
-    assert L.fattn_bwd_workspace_size(2, 3, 300, 128) == pad(6 * 384 * 128 * 4) + 2 * pad(6 * 384 * 4)
-    assert L.fattn_bwd_workspace_size(1, 1, 1, 64) == pad(128 * 64 * 4) + 2 * pad(128 * 4)
+    assert L.fattn_bwd_workspace_size(1, 32, 8192, 64) == pad(32 * 8192 * 64 * 4) + 2 * pad(32 * 8192 * 32)
+    assert L.fattn_bwd_workspace_size(2, 3, 300, 128) == pad(6 * 384 * 128 * 4) + 2 * pad(6 * 384 * 32)
+    assert L.fattn_bwd_workspace_size(1, 1, 1, 64) == pad(128 * 64 * 4) + 2 * pad(128 * 32)
     assert L.fattn_bwd_workspace_size(0, 1, 8, 64) == 0
 
 
