@@ -41,6 +41,7 @@ FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "prefill_sm103a.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "decode_sm103a.cu")
+BACKWARD_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "backward_sm103a.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -98,7 +99,8 @@ def source_digest(path):
 def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, or None when the kernel source has
     changed since the counters were taken.  Lines: `<kernel> <source-sha16> <bytes_per_launch>`."""
-    src = {"prefill": PREFILL_KERNEL_SRC, "decode": DECODE_KERNEL_SRC}[kernel]
+    src = {"prefill": PREFILL_KERNEL_SRC, "decode": DECODE_KERNEL_SRC, "backward64": BACKWARD_KERNEL_SRC,
+           "backward128": BACKWARD_KERNEL_SRC}[kernel]
     try:
         digest = source_digest(src)
         with open(TRAFFIC_FILE) as f:
@@ -551,7 +553,9 @@ def run_backward(args):
         "roofline": {"kernel": f"fattn_bwd (bwd_prep_kernel<{d}> + bwd_kernel<{d}> + bwd_dq_kernel<{d}>)",
                      "bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
-                     "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM)", "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM)",
+                     "traffic": recorded_traffic(f"backward{d}") if (B, H, N) == (1, 32, 8192) else None,
+                     "traffic_kernel": f"bwd_kernel<{d}> alone (ncu)",
                      "algorithmic_bytes": backward_bytes(B, H, N, d)},
         "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler is not None else None,
