@@ -60,17 +60,16 @@ def _load():
         lib.oracle_online_softmax.restype = None
         lib.oracle_online_normalizer.argtypes = [_D, ctypes.c_int64, _D, _D]
         lib.oracle_online_normalizer.restype = None
-        lib.oracle_attention.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int64] * 5 + [
-            ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.oracle_attention.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int64] * 7 + [
+            ctypes.c_double, ctypes.c_int]
         lib.oracle_attention.restype = ctypes.c_int64
         lib.oracle_attention_rows.argtypes = [_D, _D, _D, _I64, ctypes.c_int64, _D, _D] + [
-            ctypes.c_int64] * 5 + [ctypes.c_int, ctypes.c_double, ctypes.c_int]
+            ctypes.c_int64] * 7 + [ctypes.c_double, ctypes.c_int]
         lib.oracle_attention_rows.restype = ctypes.c_int64
-        lib.oracle_attention_probs.argtypes = [_D, _D] + [ctypes.c_int64] * 3 + [
-            ctypes.c_int, ctypes.c_double, _D]
+        lib.oracle_attention_probs.argtypes = [_D, _D] + [ctypes.c_int64] * 5 + [ctypes.c_double, _D]
         lib.oracle_attention_probs.restype = None
-        lib.oracle_attention_backward.argtypes = [_D] * 7 + [ctypes.c_int64] * 5 + [
-            ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.oracle_attention_backward.argtypes = [_D] * 7 + [ctypes.c_int64] * 7 + [
+            ctypes.c_double, ctypes.c_int]
         lib.oracle_attention_backward.restype = None
         _lib = lib
         return lib
@@ -114,6 +113,18 @@ def online_normalizer(x) -> tuple[float, float]:
     return g.value, s.value
 
 
+def band(causal: bool = False, window=None) -> tuple[int, int]:
+    """The mask as (window_left, window_right), bottom-right aligned; -1 = unbounded on that side.
+    ``window`` overrides ``causal``: no mask is (-1, -1), causal is (-1, 0), a sliding window of W
+    keys is (W - 1, 0)."""
+    if window is not None:
+        wl, wr = (int(window[0]), int(window[1]))
+        if wl < -1 or wr < -1:
+            raise ValueError("window sides must be >= -1")
+        return wl, wr
+    return (-1, 0) if causal else (-1, -1)
+
+
 def _shape4(q, k, v):
     q, k, v = _f64(q), _f64(k), _f64(v)
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
@@ -124,25 +135,27 @@ def _shape4(q, k, v):
     return q, k, v, B, H, Nq, k.shape[2], d
 
 
-def attention(q, k, v, causal: bool = False, scale: float | None = None, nthreads: int | None = None):
+def attention(q, k, v, causal: bool = False, scale: float | None = None, nthreads: int | None = None,
+              window=None):
     """O = softmax(scale*QK^T + mask) V and L = m + log l for every row, by definition.
 
-    q: [B,H,Nq,d], k,v: [B,H,Nk,d] (any float dtype; computed in fp64).  Causal masking is
-    bottom-right aligned: row i sees key j iff j <= i + Nk - Nq.  Returns (o [B,H,Nq,d],
-    lse [B,H,Nq]) as float64.
+    q: [B,H,Nq,d], k,v: [B,H,Nk,d] (any float dtype; computed in fp64).  Masks are bottom-right
+    aligned bands (see band()); causal: row i sees key j iff j <= i + Nk - Nq.  A row with no
+    visible key gets o = 0 and lse = -inf.  Returns (o [B,H,Nq,d], lse [B,H,Nq]) as float64.
     """
     q, k, v, B, H, Nq, Nk, d = _shape4(q, k, v)
     if scale is None:
         scale = 1.0 / np.sqrt(d)
+    wl, wr = band(causal, window)
     o = np.empty((B, H, Nq, d), dtype=np.float64)
     lse = np.empty((B, H, Nq), dtype=np.float64)
-    _load().oracle_attention(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d,
-                             1 if causal else 0, float(scale), nthreads or default_threads())
+    _load().oracle_attention(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d, wl, wr,
+                             float(scale), nthreads or default_threads())
     return o, lse
 
 
 def attention_rows(q, k, v, rows, causal: bool = False, scale: float | None = None,
-                   nthreads: int | None = None):
+                   nthreads: int | None = None, window=None):
     """The same definition for selected flat row indices r = (b*H + h)*Nq + i.
 
     Returns (o [len(rows), d], lse [len(rows)]).
@@ -155,13 +168,14 @@ def attention_rows(q, k, v, rows, causal: bool = False, scale: float | None = No
         raise IndexError("row index out of range")
     o = np.empty((rows.size, d), dtype=np.float64)
     lse = np.empty((rows.size,), dtype=np.float64)
+    wl, wr = band(causal, window)
     _load().oracle_attention_rows(_p(q), _p(k), _p(v), rows.ctypes.data_as(_I64), rows.size,
-                                  _p(o), _p(lse), B, H, Nq, Nk, d, 1 if causal else 0,
-                                  float(scale), nthreads or default_threads())
+                                  _p(o), _p(lse), B, H, Nq, Nk, d, wl, wr, float(scale),
+                                  nthreads or default_threads())
     return o, lse
 
 
-def attention_probs(q, k, causal: bool = False, scale: float | None = None) -> np.ndarray:
+def attention_probs(q, k, causal: bool = False, scale: float | None = None, window=None) -> np.ndarray:
     """P = softmax(scale*QK^T + mask) for one head; q [Nq,d], k [Nk,d] -> [Nq,Nk]."""
     q, k = _f64(q), _f64(k)
     Nq, d = q.shape
@@ -169,12 +183,13 @@ def attention_probs(q, k, causal: bool = False, scale: float | None = None) -> n
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     p = np.empty((Nq, Nk), dtype=np.float64)
-    _load().oracle_attention_probs(_p(q), _p(k), Nq, Nk, d, 1 if causal else 0, float(scale), _p(p))
+    wl, wr = band(causal, window)
+    _load().oracle_attention_probs(_p(q), _p(k), Nq, Nk, d, wl, wr, float(scale), _p(p))
     return p
 
 
 def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = None,
-                       nthreads: int | None = None):
+                       nthreads: int | None = None, window=None):
     """Gradients (dq, dk, dv) of O = softmax(scale*QK^T + mask) V for an upstream gradient do,
     by definition ("Flash Attention: The Hidden Gem", Phase 2), with the factor scale on dq and dk
     from X = scale * Q K^T.  Shapes as in attention(); returns float64 arrays."""
@@ -187,6 +202,7 @@ def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = 
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
+    wl, wr = band(causal, window)
     _load().oracle_attention_backward(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv), B, H, Nq, Nk, d,
-                                      1 if causal else 0, float(scale), nthreads or default_threads())
+                                      wl, wr, float(scale), nthreads or default_threads())
     return dq, dk, dv
