@@ -18,7 +18,9 @@ __all__ = [
     "FattnError",
     "fattn_fwd",
     "fattn_bwd",
+    "fattn_bwd_masked",
     "fattn_bwd_workspace_size",
+    "fattn_fwd_masked",
     "fattn_decode",
     "fattn_decode_static",
     "fattn_decode_num_splits",
@@ -58,10 +60,14 @@ def lib() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     L.fattn_fwd.restype = i
+    L.fattn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.fattn_fwd_masked.restype = i
     L.fattn_bwd_workspace_size.argtypes = [i, i, i, i]
     L.fattn_bwd_workspace_size.restype = sz
     L.fattn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, sz, vp]
     L.fattn_bwd.restype = i
+    L.fattn_bwd_masked.argtypes = [vp] * 9 + [i, i, i, i, i, i, i, f, vp, sz, vp]
+    L.fattn_bwd_masked.restype = i
     L.fattn_decode_num_splits.argtypes = [i, i]
     L.fattn_decode_num_splits.restype = i
     L.fattn_decode_workspace_size.argtypes = [i, i, i, i, i]
@@ -106,11 +112,12 @@ def _check(t, name, dtype=None):
 
 
 def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-              stream=None, want_lse: bool = True):
+              stream=None, want_lse: bool = True, window=None):
     """O = softmax(scale * Q K^T + mask) V and L per row, via the fused sm_103a kernel.
 
     q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; d in {64, 128}.  Causal masking is bottom-right
-    aligned.  Returns (out bf16 [B,H,Nq,d], lse fp32 [B,H,Nq] or None).
+    aligned.  ``window=(window_left, window_right)`` selects a banded mask instead (fattn_fwd_masked;
+    -1 = unbounded side).  Returns (out bf16 [B,H,Nq,d], lse fp32 [B,H,Nq] or None).
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -130,6 +137,13 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if lse is not None:
         _check(lse, "lse", torch.float32)
+    if window is not None:
+        st = lib().fattn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d,
+                                    int(window[0]), int(window[1]), float(scale), _stream_handle(stream, q.device))
+        if st != FATTN_OK:
+            raise FattnError(st, "fattn_fwd_masked")
+        return out, lse
     st = lib().fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d,
                          1 if causal else 0, float(scale), _stream_handle(stream, q.device))
@@ -143,7 +157,7 @@ def fattn_bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
 
 
 def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,
-              dv=None, workspace=None, stream=None):
+              dv=None, workspace=None, stream=None, window=None):
     """Gradients (dq, dk, dv) of the attention forward for an upstream gradient ``dout``.
 
     q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; out (bf16) and lse (fp32 [B,H,Nq]) are the forward's
@@ -173,6 +187,14 @@ def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None
     dv = torch.empty_like(v) if dv is None else dv
     for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, torch.bfloat16)
+    if window is not None:
+        st = lib().fattn_bwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk,
+                                    d, int(window[0]), int(window[1]), float(scale), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+        if st != FATTN_OK:
+            raise FattnError(st, "fattn_bwd_masked")
+        return dq, dk, dv
     st = lib().fattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
                          1 if causal else 0, float(scale), workspace.data_ptr(),

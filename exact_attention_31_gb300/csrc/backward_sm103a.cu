@@ -136,7 +136,8 @@ struct BArgs {
   __nv_bfloat16* dv;
   const __nv_bfloat16* ext_q;   // [BH][Nq_pad][16]  terms of -L / scale
   const __nv_bfloat16* ext_do;  // [BH][Nq_pad][16]  terms of -D
-  int BH, Nq, Nk, Nq_pad, NqT, causal, off;
+  int BH, Nq, Nk, Nq_pad, NqT;
+  int wl, wr, off;  // mask band: key j visible to query i iff i+off-wl <= j <= i+off+wr (-1 = unbounded)
   float c_log2;  // scale * log2(e)
   float scale;
   unsigned int* status;
@@ -235,10 +236,11 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
         if (lane == 0) mbar_arrive(sbar + 8 * C::kDPFree);
       }
       // s = S'^T = S^T - L / scale and dp = dP'^T = dP^T - D for queries [q0 + qa, q0 + qa + 32).
-      // Causal: key kidx is visible to query q iff kidx <= q + off.  Elements e < fv of this chunk
-      // are masked.
-      const int fv = a.causal ? kidx - a.off - (q0 + qa) : -1;
-      const bool mask = __any_sync(0xffffffffu, fv > 0);
+      // Key kidx is visible to query q iff kidx - off - wr <= q <= kidx - off + wl: elements e of
+      // this chunk outside [e_lo, e_hi] are masked.
+      const int e_lo = a.wr >= 0 ? kidx - a.off - a.wr - (q0 + qa) : -1;
+      const int e_hi = a.wl >= 0 ? kidx - a.off + a.wl - (q0 + qa) : 32;
+      const bool mask = __any_sync(0xffffffffu, e_lo > 0 || e_hi < 31);
       uint32_t pp[16], pd[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
@@ -247,8 +249,8 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
         float p0 = ex2_approx(x0);
         float p1 = ex2_approx(x1);
         if (mask) {
-          p0 = (e < fv) ? 0.f : p0;
-          p1 = (e + 1 < fv) ? 0.f : p1;
+          p0 = (e < e_lo || e > e_hi) ? 0.f : p0;
+          p1 = (e + 1 < e_lo || e + 1 > e_hi) ? 0.f : p1;
         }
         float d0, d1;
         fmul2(d0, d1, p0, p1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]));
@@ -630,10 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int jt = static_cast<int>(blockIdx.x) / a.BH;
   const int bh = static_cast<int>(blockIdx.x) % a.BH;
   const int n0 = jt * kBN;
-  // Query tiles that can see any of keys [n0, n0 + 128): all of them, or under the causal mask
-  // those with a query q >= n0 - off.  Key n0 < Nk is always visible to query Nq - 1, so n >= 1.
-  const int it0 = a.causal ? max(0, n0 - a.off) / kBM : 0;
-  const int n = a.NqT - it0;
+  // Query tiles holding a query that sees any of keys [n0, n0 + 128): q in
+  // [n0 - off - wr, k_last - off + wl] clipped to [0, Nq).  None (n = 0) is possible with a band.
+  const int k_last = min(n0 + kBN, a.Nk) - 1;
+  const long long q_lo = a.wr >= 0 ? max(0LL, static_cast<long long>(n0) - a.off - a.wr) : 0LL;
+  const long long q_hi = a.wl >= 0 ? min(static_cast<long long>(a.Nq) - 1, static_cast<long long>(k_last) - a.off + a.wl)
+                                   : static_cast<long long>(a.Nq) - 1;
+  const int it0 = q_lo <= q_hi ? static_cast<int>(q_lo / kBM) : 0;
+  const int n = q_lo <= q_hi ? static_cast<int>(q_hi / kBM) + 1 - it0 : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(sbar + 8 * C::kKVFull, 1);
@@ -674,7 +680,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   Abort ab{abort_flag, a.status, globaltimer_ns() + a.timeout_ns};
 
-  if (warp < 8) {
+  if (n == 0) {
+    // No query sees these keys: dK = dV = 0, nothing else to do.
+    if (warp < 8) {
+      const int kidx = n0 + (warp & 3) * 32 + (threadIdx.x & 31);
+      if (kidx < a.Nk) {
+        const size_t row = (static_cast<size_t>(bh) * a.Nk + kidx) * D + (warp >> 2) * (D / 2);
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          reinterpret_cast<uint4*>(a.dk + row)[i] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(a.dv + row)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+  } else if (warp < 8) {
     compute_role<D>(n, it0, n0, bh, tmem, sbase, smem, a, ab);
   } else if (warp == kProducerWarp) {
     if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, &tm_do, n, it0, n0, bh, sbase, a, ab);
@@ -754,7 +773,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (g == 0) {
     const size_t ri = (static_cast<size_t>(bh) * Nq_pad + i) * 16;
-    write_terms(ext_q + ri, valid ? -lse[static_cast<size_t>(bh) * Nq + i] * inv_scale : -INFINITY);
+    // A row with no visible key (L = -inf) must give P = 0 on every key: its term is -inf as well.
+    const float L = valid ? lse[static_cast<size_t>(bh) * Nq + i] : -INFINITY;
+    write_terms(ext_q + ri, L > -INFINITY ? -L * inv_scale : -INFINITY);
     write_terms(ext_do + ri, valid ? -acc : 0.f);
   }
 }
@@ -818,7 +839,8 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
   a.Nk = p.Nk;
   a.Nq_pad = Nq_pad;
   a.NqT = Nq_pad / kBM;
-  a.causal = p.causal;
+  a.wl = p.window_left;
+  a.wr = p.window_right;
   a.off = p.Nk - p.Nq;
   a.c_log2 = p.scale * kLog2e;
   a.scale = p.scale;

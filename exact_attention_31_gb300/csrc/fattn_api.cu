@@ -131,15 +131,19 @@ const char* fattn_status_string(int status) {
   }
 }
 
-fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                       int Nq, int Nk, int d, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace fattn {
+namespace {
+
+fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                      int Nk, int d, int wl, int wr, float scale, void* stream) {
   if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return FATTN_ERR_INVALID_ARG;
   if (!positive_sizes(B, H, Nq, Nk)) return FATTN_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FATTN_ERR_INVALID_ARG;
-  if (causal && Nq > Nk) return FATTN_ERR_INVALID_ARG;
+  if (wl < -1 || wr < -1) return FATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 0x7fffffffLL / 64) return FATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
@@ -150,30 +154,23 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
-  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, test_drop_kv_block()};
+  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, wl, wr, scale, test_drop_kv_block()};
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
   return FATTN_OK;
 }
 
-size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d) {
-  if (!positive_sizes(B, H, Nq, d)) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * bwd_padded_rows(Nq);
-  return align_up(rows * d * sizeof(float), 256) + 2 * align_up(rows * 32, 256);
-}
-
-fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
-                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, int wl,
+                      int wr, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return FATTN_ERR_INVALID_ARG;
   if (!positive_sizes(B, H, Nq, Nk)) return FATTN_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FATTN_ERR_INVALID_ARG;
-  if (causal && Nq > Nk) return FATTN_ERR_INVALID_ARG;
+  if (wl < -1 || wr < -1) return FATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 0x7fffffffLL / 256) return FATTN_ERR_INVALID_ARG;
   if (Nq > 0x7fffffff - 128) return FATTN_ERR_INVALID_ARG;
@@ -194,11 +191,51 @@ fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* 
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
-  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, causal, scale, ws_dq, ws_ext_q, ws_ext_do};
+  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, wl, wr, scale, ws_dq, ws_ext_q, ws_ext_do};
   if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
   return FATTN_OK;
+}
+
+}  // namespace
+}  // namespace fattn
+
+extern "C" {
+
+fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                       int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  if (causal != 0 && causal != 1) return FATTN_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, -1, causal ? 0 : -1, scale, stream);
+}
+
+fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int Nq, int Nk, int d, int window_left, int window_right, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, window_left, window_right, scale, stream);
+}
+
+size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d) {
+  if (!positive_sizes(B, H, Nq, d)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * bwd_padded_rows(Nq);
+  return align_up(rows * d * sizeof(float), 256) + 2 * align_up(rows * 32, 256);
+}
+
+fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (causal != 0 && causal != 1) return FATTN_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, -1, causal ? 0 : -1, scale, workspace,
+                  workspace_bytes, stream);
+}
+
+fattn_status fattn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                              int window_left, int window_right, float scale, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, window_left, window_right, scale, workspace,
+                  workspace_bytes, stream);
 }
 
 int fattn_decode_num_splits(int Nk, int num_splits) {

@@ -19,7 +19,10 @@ struct FwdProblem {
   const void* v;
   void* o;
   float* lse;
-  int B, H, Nq, Nk, d, causal;
+  int B, H, Nq, Nk, d;
+  // Band mask, bottom-right aligned: row i sees key j iff i+off-window_left <= j <= i+off+window_right
+  // with off = Nk - Nq; -1 leaves that side unbounded.  No mask (-1, -1); causal (-1, 0).
+  int window_left, window_right;
   float scale;
   // Failure-detection testing only (never set in normal use): the key tile of this block index is
   // not loaded, so the waits for it must give up and report a timeout.  -1 = off.
@@ -49,7 +52,8 @@ struct BwdProblem {
   void* dq;
   void* dk;
   void* dv;
-  int B, H, Nq, Nk, d, causal;
+  int B, H, Nq, Nk, d;
+  int window_left, window_right;  // band mask as in FwdProblem
   float scale;
   float* ws_dq;    // [B*H][Nq_pad][d] fp32 dQ accumulator
   void* ws_ext_q;   // [B*H][Nq_pad][16] bf16: three terms of -L / scale (per query row)

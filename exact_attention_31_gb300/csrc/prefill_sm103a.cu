@@ -79,7 +79,8 @@ struct Cfg {
 struct Args {
   __nv_bfloat16* o;
   float* lse;
-  int BH, Nq, Nk, causal;
+  int BH, Nq, Nk;
+  int wl, wr, off;     // mask band: key j visible to row i iff i+off-wl <= j <= i+off+wr (-1 = unbounded)
   int units_per_head;  // ceil(Nq / 256)
   float c_log2;        // scale * log2(e)
   unsigned int* status;
@@ -87,12 +88,34 @@ struct Args {
   int drop_kv_block;  // failure-detection testing only; -1 = off
 };
 
-// Number of key/value tiles query tile [r0, r0 + 128) must visit (0 if the tile is past Nq).
-__device__ __forceinline__ int tiles_needed(int r0, const Args& a) {
-  if (r0 >= a.Nq) return 0;
-  int last_key = a.Nk - 1;
-  if (a.causal) last_key = min(last_key, r0 + kBlockM - 1 + (a.Nk - a.Nq));
-  return last_key / kBlockN + 1;
+// Key/value tiles [jb, je) that query tile [r0, r0 + 128) must visit: those holding a key visible to
+// any of its rows.  Empty (jb == je) when the tile is past Nq or the band leaves it no key.
+__device__ __forceinline__ void key_tiles(int r0, const Args& a, int& jb, int& je) {
+  jb = je = 0;
+  if (r0 >= a.Nq) return;
+  const int r1 = min(r0 + kBlockM, a.Nq) - 1;
+  const long long lo = a.wl >= 0 ? max(0LL, static_cast<long long>(r0) + a.off - a.wl) : 0LL;
+  const long long hi = a.wr >= 0 ? min(static_cast<long long>(a.Nk) - 1, static_cast<long long>(r1) + a.off + a.wr)
+                                 : static_cast<long long>(a.Nk) - 1;
+  if (lo > hi) return;
+  jb = static_cast<int>(lo / kBlockN);
+  je = static_cast<int>(hi / kBlockN) + 1;
+}
+
+// First and one-past-last key tile of the union of the CTA's two query tiles' ranges (J0 >= J1 when
+// both are empty).  Each range [jb_t, je_t) is an interval, and they overlap or touch because the
+// band moves monotonically with the row.
+__host__ __device__ __forceinline__ int union_begin(const int (&jb)[2], const int (&je)[2]) {
+  int b = 0x7fffffff;
+  for (int t = 0; t < kTiles; ++t)
+    if (je[t] > jb[t]) b = min(b, jb[t]);
+  return b;
+}
+__host__ __device__ __forceinline__ int union_end(const int (&jb)[2], const int (&je)[2]) {
+  int e = 0;
+  for (int t = 0; t < kTiles; ++t)
+    if (je[t] > jb[t]) e = max(e, je[t]);
+  return e;
 }
 
 __device__ __forceinline__ void wait_dep(uint32_t (&r)[32]) {
@@ -170,13 +193,17 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t pk) {
 // Softmax group: one thread per query row.
 // ------------------------------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int bh, uint32_t tmem,
+__device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
                                              uint32_t sbar, const Args& a, const Abort& ab) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
   const int q_row = row0 + t * kBlockM + quarter * 32 + lane;
-  const int limit = a.causal ? min(q_row + (a.Nk - a.Nq), a.Nk - 1) : a.Nk - 1;
+  // this row's visible keys: [lo, hi] (lo may be negative, hi may be below lo)
+  const long long c_row = static_cast<long long>(q_row) + a.off;
+  const int hi = static_cast<int>(a.wr >= 0 ? min(c_row + a.wr, static_cast<long long>(a.Nk) - 1)
+                                            : static_cast<long long>(a.Nk) - 1);
+  const int lo = static_cast<int>(a.wl >= 0 ? max(c_row - a.wl, -1LL) : -1LL);
   const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t tS = tmem + lane_field + C::col_s(t);
   const uint32_t tO = tmem + lane_field + C::col_o(t);
@@ -187,8 +214,9 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
   float l = 0.f;            // sum of the fp32 weights: L = m + log(l)
   float lr = 0.f;           // sum of the bf16-rounded weights that entered P V: O = O / lr
   bool ok = true;
-  for (int j = 0; j < n_tiles; ++j) {
-    if (!warp_wait(sbar + 8 * (C::kSFull + t), j & 1, ab)) {
+  for (int k = 0; k < n_tiles; ++k) {
+    const int j = jb + k;
+    if (!warp_wait(sbar + 8 * (C::kSFull + t), k & 1, ab)) {
       ok = false;
       break;
     }
@@ -206,12 +234,12 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
     }
 
     const int kv0 = j * kBlockN;
-    if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > limit)) {
+    if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > hi || kv0 < lo)) {
 #pragma unroll
       for (int h = 0; h < 4; ++h)
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (kv0 + 32 * h + i > limit) s[h][i] = __float_as_uint(-INFINITY);
+          if (kv0 + 32 * h + i > hi || kv0 + 32 * h + i < lo) s[h][i] = __float_as_uint(-INFINITY);
     }
     // row max: eight independent three-input chains
     float mx8[8];
@@ -260,8 +288,8 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
 
     if constexpr (C::kSepP) {
       // P_t and O_t are still read by P_t(j-1) V_{j-1} until it completes.
-      if (j > 0) {
-        if (!warp_wait(sbar + 8 * (C::kPVDone + t), (j - 1) & 1, ab)) {
+      if (k > 0) {
+        if (!warp_wait(sbar + 8 * (C::kPVDone + t), (k - 1) & 1, ab)) {
           ok = false;
           break;
         }
@@ -272,7 +300,7 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
     tmem_st_32x32b_x32(tP + 32, p[1]);
 
     // Rescale O_t (last written by P_t(j-1) V_{j-1}, now complete) when the reference moved.
-    if (j > 0 && __any_sync(0xffffffffu, need)) {
+    if (k > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int h = 0; h < D / 32; ++h) {
         uint32_t o[32];
@@ -293,13 +321,24 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
     __syncwarp();
     if (lane == 0) mbar_arrive(sbar + 8 * (C::kPFull + t));
   }
-  if (!ok || n_tiles == 0) return;
+  if (!ok) return;
+  const bool store = q_row < a.Nq;
+  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
+  if (n_tiles == 0) {
+    // No key is visible to any row of this tile: o = 0, L = log(0) = -inf.
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (a.lse != nullptr) a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = -INFINITY;
+    }
+    return;
+  }
 
   if (!warp_wait(sbar + 8 * (C::kOFull + t), 0, ab)) return;
   tc_fence_after();
-  const float inv_l = 1.f / lr;
-  const bool store = q_row < a.Nq;
-  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
+  // A row that saw no key has l = lr = 0 and m = -inf: o = 0 and L = -inf.
+  const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
 #pragma unroll
   for (int h = 0; h < D / 32; ++h) {
     uint32_t o[32];
@@ -316,7 +355,7 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
     }
   }
   if (store && a.lse != nullptr) {
-    a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+    a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
 }
 
@@ -325,8 +364,9 @@ __device__ __forceinline__ void softmax_role(int t, int n_tiles, int row0, int b
 // ------------------------------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk,
-                                              const CUtensorMap* tv, const int (&n)[2], int row0,
-                                              int bh, uint32_t sbase, int drop_kv_block, const Abort& ab) {
+                                              const CUtensorMap* tv, const int (&jb)[2], const int (&je)[2],
+                                              int row0, int bh, uint32_t sbase, int drop_kv_block,
+                                              const Abort& ab) {
   using C = Cfg<D>;
   const uint32_t sbar = sbase + C::kBarOff;
   tma_prefetch_desc(tq);
@@ -334,7 +374,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
   tma_prefetch_desc(tv);
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
-    if (n[t] == 0) continue;
+    if (je[t] == jb[t]) continue;
     const uint32_t bar = sbar + 8 * (C::kQFull + t);
     mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
@@ -342,14 +382,15 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
       tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + ch * kAtomBytes, tq, bar, ch * 64,
                   row0 + t * kBlockM, bh);
   }
-  const int nmax = max(n[0], n[1]);
+  // K_j and V_j for the union of the two tiles' ranges; ring index 2 (j - J0) + w
+  const int J0 = union_begin(jb, je), J1 = union_end(jb, je);
   int issued = 0;   // ring index one past the last load issued
   int dropped = -1; // ring index of the load skipped for failure-detection testing
   bool ok = true;
-  for (int j = 0; j < nmax && ok; ++j) {
+  for (int j = J0; j < J1 && ok; ++j) {
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
-      const int idx = 2 * j + w;
+      const int idx = 2 * (j - J0) + w;
       const int slot = idx % C::kSlots;
       const int round = idx / C::kSlots;
       if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) {
@@ -437,46 +478,51 @@ struct MmaCtx {
 };
 
 // Separate P (d = 64): S_t(j+1) is issued once S_t(j) has been read, P_t(j) V_j once P_t(j) is written.
+// Tile t visits key tiles [jb_t, je_t); its barriers count its own steps k = j - jb_t.
 template <int D>
-__device__ __forceinline__ bool mma_loop_separate_p(const int (&n)[2], const MmaCtx<D>& m, const Abort& ab) {
+__device__ __forceinline__ bool mma_loop_separate_p(const int (&jb)[2], const int (&je)[2], const MmaCtx<D>& m,
+                                                    const Abort& ab) {
   using C = Cfg<D>;
-  const int nmax = max(n[0], n[1]);
-  if (nmax == 0) return true;
+  const int J0 = union_begin(jb, je), J1 = union_end(jb, je);
+  if (J0 >= J1) return true;
+  auto active = [&](int t, int j) { return jb[t] <= j && j < je[t]; };
   if (!m.wait_kv(0, ab)) return false;
   tc_fence_after();
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
-    if (n[t] > 0) {
+    if (active(t, J0)) {
       m.issue_s(t, 0);
       m.commit(C::kSFull + t);
     }
   }
-  m.commit(C::kKVEmpty + 0);  // K_0 (slot 0) is free once both S(0) are done
-  for (int j = 0; j < nmax; ++j) {
-    if (j + 1 < nmax) {
-      const int kidx = 2 * (j + 1);
+  m.commit(C::kKVEmpty + 0);  // K_{J0} (slot 0) is free once the S(J0) are done
+  for (int j = J0; j < J1; ++j) {
+    if (j + 1 < J1) {
+      const int kidx = 2 * (j + 1 - J0);
       if (!m.wait_kv(kidx, ab)) return false;
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
-        if (j + 1 < n[t]) {
-          if (!m.wait(C::kSFree + t, j, ab)) return false;
-          tc_fence_after();
+        if (active(t, j + 1)) {
+          if (j + 1 > jb[t]) {  // S_t(j) must have been read first
+            if (!m.wait(C::kSFree + t, j - jb[t], ab)) return false;
+            tc_fence_after();
+          }
           m.issue_s(t, kidx % C::kSlots);
           m.commit(C::kSFull + t);
         }
       }
       m.commit(C::kKVEmpty + kidx % C::kSlots);
     }
-    const int vidx = 2 * j + 1;
+    const int vidx = 2 * (j - J0) + 1;
     if (!m.wait_kv(vidx, ab)) return false;
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-      if (j < n[t]) {
-        if (!m.wait(C::kPFull + t, j, ab)) return false;
+      if (active(t, j)) {
+        if (!m.wait(C::kPFull + t, j - jb[t], ab)) return false;
         tc_fence_after();
-        m.issue_pv(t, vidx % C::kSlots, j == 0);
+        m.issue_pv(t, vidx % C::kSlots, j == jb[t]);
         m.commit(C::kPVDone + t);
-        if (j == n[t] - 1) m.commit(C::kOFull + t);
+        if (j == je[t] - 1) m.commit(C::kOFull + t);
       }
     }
     m.commit(C::kKVEmpty + vidx % C::kSlots);
@@ -487,43 +533,48 @@ __device__ __forceinline__ bool mma_loop_separate_p(const int (&n)[2], const Mma
 // P aliased over S (d = 128): S_t(j+1) is issued after P_t(j) V_j, which reads P_t from the same
 // columns (tcgen05.mma operations of one CTA execute in issue order).
 template <int D>
-__device__ __forceinline__ bool mma_loop_aliased_p(const int (&n)[2], const MmaCtx<D>& m, const Abort& ab) {
+__device__ __forceinline__ bool mma_loop_aliased_p(const int (&jb)[2], const int (&je)[2], const MmaCtx<D>& m,
+                                                   const Abort& ab) {
   using C = Cfg<D>;
-  const int nmax = max(n[0], n[1]);
-  for (int j = 0; j <= nmax; ++j) {
-    if (j < nmax && !m.wait_kv(2 * j, ab)) return false;
-    if (j > 0 && !m.wait_kv(2 * (j - 1) + 1, ab)) return false;
+  const int J0 = union_begin(jb, je), J1 = union_end(jb, je);
+  if (J0 >= J1) return true;
+  auto active = [&](int t, int j) { return jb[t] <= j && j < je[t]; };
+  for (int j = J0; j <= J1; ++j) {
+    const int r = j - J0;  // ring step
+    if (j < J1 && !m.wait_kv(2 * r, ab)) return false;
+    if (j > J0 && !m.wait_kv(2 * (r - 1) + 1, ab)) return false;
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-      if (j > 0 && j - 1 < n[t]) {
-        if (!m.wait(C::kPFull + t, j - 1, ab)) return false;
+      if (j > J0 && active(t, j - 1)) {
+        if (!m.wait(C::kPFull + t, j - 1 - jb[t], ab)) return false;
         tc_fence_after();
-        m.issue_pv(t, (2 * (j - 1) + 1) % C::kSlots, j == 1);
-        if (j - 1 == n[t] - 1) m.commit(C::kOFull + t);
+        m.issue_pv(t, (2 * (r - 1) + 1) % C::kSlots, j - 1 == jb[t]);
+        if (j - 1 == je[t] - 1) m.commit(C::kOFull + t);
       }
-      if (j < n[t]) {
-        m.issue_s(t, (2 * j) % C::kSlots);
+      if (j < J1 && active(t, j)) {
+        m.issue_s(t, (2 * r) % C::kSlots);
         m.commit(C::kSFull + t);
       }
     }
-    if (j < nmax) m.commit(C::kKVEmpty + (2 * j) % C::kSlots);
-    if (j > 0) m.commit(C::kKVEmpty + (2 * (j - 1) + 1) % C::kSlots);
+    if (j < J1) m.commit(C::kKVEmpty + (2 * r) % C::kSlots);
+    if (j > J0) m.commit(C::kKVEmpty + (2 * (r - 1) + 1) % C::kSlots);
   }
   return true;
 }
 
 // Whole warp.
 template <int D>
-__device__ __forceinline__ void mma_role(const int (&n)[2], uint32_t tmem, uint32_t sbase, const Abort& ab) {
+__device__ __forceinline__ void mma_role(const int (&jb)[2], const int (&je)[2], uint32_t tmem, uint32_t sbase,
+                                         const Abort& ab) {
   using C = Cfg<D>;
   MmaCtx<D> m;
   m.init(tmem, sbase);
   bool ok = true;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t)
-    if (n[t] > 0 && ok) ok = m.wait(C::kQFull + t, 0, ab);
-  if (ok) ok = C::kSepP ? mma_loop_separate_p<D>(n, m, ab) : mma_loop_aliased_p<D>(n, m, ab);
+    if (je[t] > jb[t] && ok) ok = m.wait(C::kQFull + t, 0, ab);
+  if (ok) ok = C::kSepP ? mma_loop_separate_p<D>(jb, je, m, ab) : mma_loop_aliased_p<D>(jb, je, m, ab);
   // Before the CTA winds down, every MMA (and every arrival its commits make on this CTA's
   // barriers) has completed, on the normal path and after a timeout alike.
   m.commit(C::kDrain);
@@ -551,9 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit = a.units_per_head - 1 - static_cast<int>(blockIdx.x) / a.BH;
   const int bh = static_cast<int>(blockIdx.x) % a.BH;
   const int row0 = unit * kTiles * kBlockM;
-  int n[2];
-  n[0] = tiles_needed(row0, a);
-  n[1] = tiles_needed(row0 + kBlockM, a);
+  int jb[2], je[2];
+  key_tiles(row0, a, jb[0], je[0]);
+  key_tiles(row0 + kBlockM, a, jb[1], je[1]);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < kTiles; ++t) {
@@ -584,12 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     const int t = warp >> 2;
-    softmax_role<D>(t, n[t], row0, bh, tmem, sbar, a, ab);
+    softmax_role<D>(t, jb[t], je[t] - jb[t], row0, bh, tmem, sbar, a, ab);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, n, row0, bh, sbase, a.drop_kv_block, ab);
+    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, jb, je, row0, bh, sbase, a.drop_kv_block, ab);
     __syncwarp();
   } else {
-    mma_role<D>(n, tmem, sbase, ab);
+    mma_role<D>(jb, je, tmem, sbase, ab);
   }
 
   tc_fence_before();
@@ -621,7 +672,9 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.BH = p.B * p.H;
   a.Nq = p.Nq;
   a.Nk = p.Nk;
-  a.causal = p.causal;
+  a.wl = p.window_left;
+  a.wr = p.window_right;
+  a.off = p.Nk - p.Nq;
   a.units_per_head = (p.Nq + kTiles * kBlockM - 1) / (kTiles * kBlockM);
   a.c_log2 = p.scale * 1.4426950408889634f;
   a.status = status;

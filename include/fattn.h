@@ -63,6 +63,22 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int Nq, int Nk, int d, int causal, float scale, void* stream);
 
 /*
+ * fattn_fwd_masked -- fattn_fwd with a banded mask ("Understanding FlashAttention", Attention: a
+ * mask is elementwise and independent of the scores, causal masking being one kind among others;
+ * What is left to the implementation, point 2: rows whose keys are all masked).
+ *
+ * With off = Nk - Nq, query row i sees key j iff
+ *     i + off - window_left  <=  j  <=  i + off + window_right,
+ * where -1 leaves that side unbounded.  No mask is (-1, -1), causal is (-1, 0) (the same as
+ * fattn_fwd with causal = 1), a sliding window of the last W keys is (W - 1, 0).  Any Nq, Nk >= 1
+ * is accepted.  A row with no visible key gets o = 0 and L = -inf (log of an empty sum).
+ * Returns FATTN_ERR_INVALID_ARG for a window side below -1; other arguments as for fattn_fwd.
+ */
+fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int Nq, int Nk, int d, int window_left, int window_right, float scale,
+                              void* stream);
+
+/*
  * fattn_bwd -- gradients of the attention forward ("Flash Attention: The Hidden Gem", Phase 2:
  * Chain Rule Through a Matrix Multiply, The Softmax Jacobian, The D Shortcut, The Algorithm).
  *
@@ -93,6 +109,16 @@ size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d);
 fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
                        int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fattn_bwd_masked -- fattn_bwd for the banded masks of fattn_fwd_masked (same window_left,
+ * window_right, o and lse as that call produced).  Rows with no visible key get dq = 0; keys that
+ * no query sees get dk = dv = 0.
+ */
+fattn_status fattn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                              int window_left, int window_right, float scale, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /*
  * fattn_decode_num_splits -- the number of key splits fattn_decode uses for a request.
