@@ -58,6 +58,17 @@ def prefill_bytes(B, H, N, d):
     return B * H * N * d * 2 * 4 + B * H * N * 4
 
 
+def visible_pairs(N, window_left=-1):
+    """(query, key) pairs a causal prefill of N rows computes, with an optional sliding window of
+    window_left + 1 keys (band (window_left, 0), Nq == Nk)."""
+    if window_left < 0:
+        return N * (N + 1) / 2
+    W = window_left + 1
+    if W >= N:
+        return N * (N + 1) / 2
+    return W * (W + 1) / 2 + (N - W) * W
+
+
 def backward_flops(B, H, N, d, causal):
     # the five products of the backward (S, dP, dV, dK, dQ), 2*N*N*d each; half under the causal mask
     f = 10.0 * B * H * N * N * d
@@ -322,6 +333,7 @@ def run_ours(args):
     seed = 0xFA77E000
     stream = torch.cuda.current_stream(dev)
     scale_p, scale_d = 1 / math.sqrt(P["d"]), 1 / math.sqrt(D["d"])
+    window = (args.window, 0) if args.window >= 0 else None
     if do_prefill:
         q, k, v, _ = make_qkv(P["B"], P["H"], P["N"], P["N"], P["d"], seed + 4, dev)
         o = torch.empty_like(q)
@@ -339,7 +351,7 @@ def run_ours(args):
             flush.zero_()
             if evs is not None:
                 evs[0].record(stream)
-            fa.fattn_fwd(q, k, v, causal=True, scale=scale_p, out=o, lse=lse, stream=stream)
+            fa.fattn_fwd(q, k, v, causal=True, scale=scale_p, out=o, lse=lse, stream=stream, window=window)
             if evs is not None:
                 evs[1].record(stream)
         if do_decode:
@@ -400,6 +412,8 @@ def run_ours(args):
         return
     peaks, peak_src = load_peaks()
     pf = prefill_flops(P["B"], P["H"], P["N"], P["d"], True)
+    if args.window >= 0:
+        pf = 4.0 * P["B"] * P["H"] * P["d"] * visible_pairs(P["N"], args.window)
     kv = decode_kv_bytes(D["B"], D["H"], D["Nk"], D["d"])
     line = {"metric": METRIC}
     if do_prefill:
@@ -407,6 +421,8 @@ def run_ours(args):
     else:
         line.update(value=round(world * kv / (dec_avg * 1e-3) / 1e9, 1), unit="GB/s")
     name_p = f"prefill_b{P['B']}h{P['H']}_n{P['N']}_d{P['d']} causal"
+    if args.window >= 0:
+        name_p += f" sliding window {args.window + 1}"
     name_d = f"decode_b{D['B']}h{D['H']}_nk{D['Nk']}_d{D['d']}"
     workload = " + ".join(([name_p] if do_prefill else []) + ([name_d] if do_decode else []))
     line.update({
@@ -429,7 +445,8 @@ def run_ours(args):
     if do_prefill:
         per_launch = pf / (pre_avg * 1e-3) / 1e12
         line["config"]["prefill"] = {"B": P["B"], "H": P["H"], "Nq": P["N"], "Nk": P["N"], "d": P["d"],
-                                     "causal": True, "scale": scale_p, "flops_per_launch": pf}
+                                     "causal": True, "scale": scale_p, "flops_per_launch": pf,
+                                     "window": None if args.window < 0 else [args.window, 0]}
         line["prefill_ms"] = round(pre_avg, 4)
         line["roofline"] = {
             "kernel": "prefill_kernel<64> (fattn_fwd)",
@@ -490,7 +507,8 @@ def run_backward(args):
     scale = 1 / math.sqrt(d)
     q, k, v, _ = make_qkv(B, H, N, N, d, seed, dev)
     do = make_dout(B, H, N, d, seed, dev)
-    o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=scale, stream=stream)
+    window = (args.window, 0) if args.window >= 0 else None
+    o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=scale, stream=stream, window=window)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fattn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -499,7 +517,7 @@ def run_backward(args):
         flush.zero_()
         if evs is not None:
             evs[0].record(stream)
-        fa.fattn_bwd(q, k, v, o, lse, do, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+        fa.fattn_bwd(q, k, v, o, lse, do, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws, window=window,
                      stream=stream)
         if evs is not None:
             evs[1].record(stream)
@@ -537,6 +555,8 @@ def run_backward(args):
         return
     peaks, peak_src = load_peaks()
     fl = backward_flops(B, H, N, d, True)
+    if args.window >= 0:
+        fl = 10.0 * B * H * d * visible_pairs(N, args.window)
     tf = fl / (avg * 1e-3) / 1e12
     line = {
         "metric": "attn bwd TFLOP/s (fattn_bwd: pre-pass + fused kernel + dQ pass)",
@@ -544,7 +564,8 @@ def run_backward(args):
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded iid N(0,1) drawn in fp32 and rounded to bf16 (q, k, v, dO)",
-        "config": {"workload": f"backward_b{B}h{H}_n{N}_d{d} causal",
+        "config": {"workload": f"backward_b{B}h{H}_n{N}_d{d} causal" +
+                               (f" sliding window {args.window + 1}" if args.window >= 0 else ""),
                    "backward": {"B": B, "H": H, "Nq": N, "Nk": N, "d": d, "causal": True, "scale": scale,
                                 "flops_per_call": fl},
                    "l2": "a 512 MiB buffer is written before every call (outside the per-call events)",
@@ -683,6 +704,8 @@ def main(argv=None):
                     help="both = the benchmark step; prefill/decode time one half (profiling); backward "
                          "times fattn_bwd on the prefill shape (a line of its own)")
     ap.add_argument("--bwd-d", type=int, default=0, help="override d of the backward workload (64 or 128)")
+    ap.add_argument("--window", type=int, default=-1,
+                    help="sliding-window band (W-1, 0) for the prefill/backward workloads (FLOPs = visible pairs)")
     ap.add_argument("--prefill-heads", type=int, default=0, help="override H of the prefill (profiling)")
     ap.add_argument("--decode-batch", type=int, default=0, help="override B of the decode (profiling)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,

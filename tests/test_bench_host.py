@@ -42,3 +42,11 @@ def test_clock_summary():
     s = bench.summarize_clocks(samples, 8.9, 8.95)
     assert s["samples"] == 1 and s["reasons"] == ["hw_slowdown"]
     assert bench.summarize_clocks([], 0, 1)["sm_mhz"] is None
+
+
+def test_visible_pairs_counts_the_band():
+    # brute-force count of (i, j) with max(0, i - W + 1) <= j <= i
+    for N, W in ((10, 4), (7, 7), (9, 20), (33, 1)):
+        brute = sum(1 for i in range(N) for j in range(N) if i - (W - 1) <= j <= i)
+        assert bench.visible_pairs(N, W - 1) == brute
+    assert bench.visible_pairs(12) == 12 * 13 / 2
