@@ -6,6 +6,12 @@
 // O by exp(m_old - m_new) (The Correction Factor), add P = exp(S - m) and P V; after the last tile
 // write O / l and L = m + log(l).  S and P live only in tensor memory.
 //
+// The grid is persistent: at most one CTA per SM, each working through units (two adjacent 128-row
+// query tiles of one (b, h)) in rounds, heaviest causal units first.  Every barrier counts its
+// phases over all of a CTA's units, so the next unit's Q tiles, K/V tiles and first S are fetched
+// and computed while the current unit finishes; two barriers guard the hand-over (the last S_t has
+// read Q_t before Q_t is reloaded; the epilogue has read O_t before the next P_t V overwrites it).
+//
 // How it maps onto one SM (one CTA per SM, 320 threads):
 //   warps 0-3  softmax group for query tile 0 (one thread per query row / TMEM lane)
 //   warps 4-7  softmax group for query tile 1
@@ -64,10 +70,12 @@ struct Cfg {
   static constexpr int kPFull = 6;              // [2] P_t written, O_t corrected
   static constexpr int kPVDone = 8;             // [2] O_t += P_t V done (separate-P only)
   static constexpr int kOFull = 10;             // [2] last P V of tile t done
-  static constexpr int kDrain = 12;             // [1] wind-down after a timeout
-  static constexpr int kKVFull = 13;            // [kSlots]
-  static constexpr int kKVEmpty = 13 + kSlots;  // [kSlots]
-  static constexpr int kNumBars = 13 + 2 * kSlots;
+  static constexpr int kQFree = 12;             // [2] the unit's last S_t has read Q_t
+  static constexpr int kOFree = 14;             // [2] O_t read out by the epilogue (one arrival per warp)
+  static constexpr int kDrain = 16;             // [1] wind-down after a timeout
+  static constexpr int kKVFull = 17;            // [kSlots]
+  static constexpr int kKVEmpty = 17 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 17 + 2 * kSlots;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
   // tensor-memory columns
@@ -82,6 +90,7 @@ struct Args {
   int BH, Nq, Nk;
   int wl, wr, off;     // mask band: key j visible to row i iff i+off-wl <= j <= i+off+wr (-1 = unbounded)
   int units_per_head;  // ceil(Nq / 256)
+  int total_units;     // BH * units_per_head
   float c_log2;        // scale * log2(e)
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -118,6 +127,27 @@ __host__ __device__ __forceinline__ int union_end(const int (&jb)[2], const int 
   return e;
 }
 
+// One unit of work: two adjacent 128-row query tiles of one (b, h), with each tile's key-tile range.
+struct Unit {
+  int bh, row0;
+  int jb[2], je[2];
+};
+
+// The k-th unit of this CTA.  The grid is persistent (at most one CTA per SM); units are taken in
+// rounds of gridDim.x, heaviest causal units (last query rows) first, and every other round is
+// walked backwards so that each CTA's total is closer to the others'.  Returns false past the end.
+__device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (idx >= a.total_units) return false;
+  const int i = static_cast<int>(idx);
+  u.bh = i % a.BH;
+  u.row0 = (a.units_per_head - 1 - i / a.BH) * kTiles * kBlockM;
+  key_tiles(u.row0, a, u.jb[0], u.je[0]);
+  key_tiles(u.row0 + kBlockM, a, u.jb[1], u.je[1]);
+  return true;
+}
+
 __device__ __forceinline__ void wait_dep(uint32_t (&r)[32]) {
   // tcgen05.wait::ld that also ties the loaded registers, so no use can be scheduled above it
   asm volatile(
@@ -137,6 +167,8 @@ struct Abort {
     *flag = 1u;
     atomicOr(status, kStatusTimeout);
   }
+  // A CTA works through many units; each role gives its waits a fresh limit at every unit.
+  __device__ void renew(unsigned long long timeout_ns) { deadline = globaltimer_ns() + timeout_ns; }
 };
 
 // Every thread of a warp waits; the outcome is made warp-uniform so the warp stays converged for
@@ -192,9 +224,11 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t pk) {
 // ------------------------------------------------------------------------------------------------
 // Softmax group: one thread per query row.
 // ------------------------------------------------------------------------------------------------
+// g counts tile t's steps over all units of this CTA (the phase of S_full, P_full, PV_done);
+// done counts its non-empty units (the phase of O_full and O_free).
 template <int D>
-__device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
-                                             uint32_t sbar, const Args& a, const Abort& ab) {
+__device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
+                                             uint32_t sbar, const Args& a, const Abort& ab, int& g, int& done) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
@@ -214,9 +248,9 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
   float l = 0.f;            // sum of the fp32 weights: L = m + log(l)
   float lr = 0.f;           // sum of the bf16-rounded weights that entered P V: O = O / lr
   bool ok = true;
-  for (int k = 0; k < n_tiles; ++k) {
-    const int j = jb + k;
-    if (!warp_wait(sbar + 8 * (C::kSFull + t), k & 1, ab)) {
+  for (int step = 0; step < n_tiles; ++step, ++g) {
+    const int j = jb + step;
+    if (!warp_wait(sbar + 8 * (C::kSFull + t), g & 1, ab)) {
       ok = false;
       break;
     }
@@ -287,9 +321,9 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
     lr += (lrs[0] + lrs[1]) + (lrs[2] + lrs[3]);
 
     if constexpr (C::kSepP) {
-      // P_t and O_t are still read by P_t(j-1) V_{j-1} until it completes.
-      if (k > 0) {
-        if (!warp_wait(sbar + 8 * (C::kPVDone + t), (k - 1) & 1, ab)) {
+      // P_t is still read by the previous P_t V until it completes.
+      if (g > 0) {
+        if (!warp_wait(sbar + 8 * (C::kPVDone + t), (g - 1) & 1, ab)) {
           ok = false;
           break;
         }
@@ -300,7 +334,7 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
     tmem_st_32x32b_x32(tP + 32, p[1]);
 
     // Rescale O_t (last written by P_t(j-1) V_{j-1}, now complete) when the reference moved.
-    if (k > 0 && __any_sync(0xffffffffu, need)) {
+    if (step > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int h = 0; h < D / 32; ++h) {
         uint32_t o[32];
@@ -321,7 +355,7 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
     __syncwarp();
     if (lane == 0) mbar_arrive(sbar + 8 * (C::kPFull + t));
   }
-  if (!ok) return;
+  if (!ok) return false;
   const bool store = q_row < a.Nq;
   __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
   if (n_tiles == 0) {
@@ -332,10 +366,10 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
       for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       if (a.lse != nullptr) a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = -INFINITY;
     }
-    return;
+    return true;
   }
 
-  if (!warp_wait(sbar + 8 * (C::kOFull + t), 0, ab)) return;
+  if (!warp_wait(sbar + 8 * (C::kOFull + t), done & 1, ab)) return false;
   tc_fence_after();
   // A row that saw no key has l = lr = 0 and m = -inf: o = 0 and L = -inf.
   const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
@@ -354,8 +388,24 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
       for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     }
   }
+  // O_t has been read: the next unit's first P_t V may overwrite it.
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sbar + 8 * (C::kOFree + t));
+  ++done;
   if (store && a.lse != nullptr) {
     a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+  return true;
+}
+
+template <int D>
+__device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab) {
+  int g = 0, done = 0;
+  Unit u;
+  for (int k = 0; cta_unit(k, a, u); ++k) {
+    ab.renew(a.timeout_ns);
+    if (!softmax_unit<D>(t, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done)) return;
   }
 }
 
@@ -364,51 +414,63 @@ __device__ __forceinline__ void softmax_role(int t, int jb, int n_tiles, int row
 // ------------------------------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk,
-                                              const CUtensorMap* tv, const int (&jb)[2], const int (&je)[2],
-                                              int row0, int bh, uint32_t sbase, int drop_kv_block,
-                                              const Abort& ab) {
+                                              const CUtensorMap* tv, uint32_t sbase, const Args& a, Abort ab) {
   using C = Cfg<D>;
   const uint32_t sbar = sbase + C::kBarOff;
   tma_prefetch_desc(tq);
   tma_prefetch_desc(tk);
   tma_prefetch_desc(tv);
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t) {
-    if (je[t] == jb[t]) continue;
-    const uint32_t bar = sbar + 8 * (C::kQFull + t);
-    mbar_arrive_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-    for (int ch = 0; ch < C::kChunks; ++ch)
-      tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + ch * kAtomBytes, tq, bar, ch * 64,
-                  row0 + t * kBlockM, bh);
-  }
-  // K_j and V_j for the union of the two tiles' ranges; ring index 2 (j - J0) + w
-  const int J0 = union_begin(jb, je), J1 = union_end(jb, je);
-  int issued = 0;   // ring index one past the last load issued
-  int dropped = -1; // ring index of the load skipped for failure-detection testing
+  int ring = 0;           // K/V ring index of the unit's first key tile (2 per key tile, over all units)
+  int qloads[2] = {0, 0}; // Q_t loads issued so far (the phase of Q_full / Q_free)
+  int issued = 0;         // ring index one past the last K/V load issued
+  int dropped = -1;       // ring index of the load skipped for failure-detection testing
   bool ok = true;
-  for (int j = J0; j < J1 && ok; ++j) {
+  Unit u;
+  for (int k = 0; ok && cta_unit(k, a, u); ++k) {
+    ab.renew(a.timeout_ns);
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const int idx = 2 * (j - J0) + w;
-      const int slot = idx % C::kSlots;
-      const int round = idx / C::kSlots;
-      if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) {
+    for (int t = 0; t < kTiles; ++t) {
+      if (u.je[t] == u.jb[t]) continue;
+      // Q_t's buffer is free once the previous unit's last S_t has read it.
+      if (qloads[t] > 0 && !thread_wait(sbar + 8 * (C::kQFree + t), (qloads[t] - 1) & 1, ab)) {
         ok = false;
         break;
       }
-      issued = idx + 1;
-      if (w == 0 && j == drop_kv_block) {  // testing only: this tile never arrives
-        dropped = idx;
-        continue;
-      }
-      const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
+      const uint32_t bar = sbar + 8 * (C::kQFull + t);
       mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
       for (int ch = 0; ch < C::kChunks; ++ch)
-        tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + ch * kAtomBytes, w ? tv : tk, bar,
-                    ch * 64, j * kBlockN, bh);
+        tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + ch * kAtomBytes, tq, bar, ch * 64,
+                    u.row0 + t * kBlockM, u.bh);
+      ++qloads[t];
     }
+    if (!ok) break;
+    // K_j and V_j for the union of the two tiles' ranges; ring index ring + 2 (j - J0) + w
+    const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
+    for (int j = J0; j < J1 && ok; ++j) {
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int idx = ring + 2 * (j - J0) + w;
+        const int slot = idx % C::kSlots;
+        const int round = idx / C::kSlots;
+        if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) {
+          ok = false;
+          break;
+        }
+        issued = idx + 1;
+        if (w == 0 && j == a.drop_kv_block) {  // testing only: this tile never arrives
+          dropped = idx;
+          continue;
+        }
+        const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
+        mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+        for (int ch = 0; ch < C::kChunks; ++ch)
+          tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + ch * kAtomBytes, w ? tv : tk, bar,
+                      ch * 64, j * kBlockN, u.bh);
+      }
+    }
+    if (J1 > J0) ring += 2 * (J1 - J0);
   }
   if (!ok) {
     // Let the copies already in flight land before the CTA's shared memory goes away.
@@ -419,6 +481,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
       const int slot = idx % C::kSlots;
       mbar_wait_bounded(sbar + 8 * (C::kKVFull + slot), (idx / C::kSlots) & 1, &never, until);
     }
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+      if (qloads[t] > 0) mbar_wait_bounded(sbar + 8 * (C::kQFull + t), (qloads[t] - 1) & 1, &never, until);
   }
 }
 
@@ -477,104 +542,132 @@ struct MmaCtx {
   }
 };
 
-// Separate P (d = 64): S_t(j+1) is issued once S_t(j) has been read, P_t(j) V_j once P_t(j) is written.
-// Tile t visits key tiles [jb_t, je_t); its barriers count its own steps k = j - jb_t.
+// Barrier phases of the MMA warp over all units of the CTA.
+struct MmaState {
+  int ring = 0;              // K/V ring index of the current unit's first key tile
+  int s_issued[2] = {0, 0};  // S_t issued (S_full commits); S_t number n waits S_free number n-1
+  int p_seen[2] = {0, 0};    // P_full phases consumed
+  int units[2] = {0, 0};     // non-empty units finished per tile (O_full commits, O_free phases)
+  int q_seen[2] = {0, 0};    // Q_full phases consumed
+};
+
+// S_t for key tile j.  The columns are free once the softmax warps have read the previous S_t (d = 64;
+// with d = 128 the previous P_t V, issued earlier by this warp, reads P_t from them).  The unit's
+// last S_t releases Q_t.
 template <int D>
-__device__ __forceinline__ bool mma_loop_separate_p(const int (&jb)[2], const int (&je)[2], const MmaCtx<D>& m,
+__device__ __forceinline__ bool issue_s_step(int t, int slot, bool last, const MmaCtx<D>& m, MmaState& st,
+                                             const Abort& ab) {
+  using C = Cfg<D>;
+  if (C::kSepP && st.s_issued[t] > 0) {
+    if (!m.wait(C::kSFree + t, st.s_issued[t] - 1, ab)) return false;
+    tc_fence_after();
+  }
+  m.issue_s(t, slot);
+  m.commit(C::kSFull + t);
+  if (last) m.commit(C::kQFree + t);
+  ++st.s_issued[t];
+  return true;
+}
+
+// O_t += P_t V_j.  The unit's first P_t V overwrites O_t: the previous unit's epilogue must have read it.
+template <int D>
+__device__ __forceinline__ bool issue_pv_step(int t, int slot, bool first, bool last, const MmaCtx<D>& m,
+                                              MmaState& st, const Abort& ab) {
+  using C = Cfg<D>;
+  if (!m.wait(C::kPFull + t, st.p_seen[t]++, ab)) return false;
+  if (first && st.units[t] > 0 && !m.wait(C::kOFree + t, st.units[t] - 1, ab)) return false;
+  tc_fence_after();
+  m.issue_pv(t, slot, first);
+  if (C::kSepP) m.commit(C::kPVDone + t);
+  if (last) {
+    m.commit(C::kOFull + t);
+    ++st.units[t];
+  }
+  return true;
+}
+
+// Separate P (d = 64): S_t(j+1) is issued once S_t(j) has been read, P_t(j) V_j once P_t(j) is written.
+// Tile t visits key tiles [jb_t, je_t); ring index of K_j is ring + 2 (j - J0), of V_j one more.
+template <int D>
+__device__ __forceinline__ bool mma_unit_separate_p(const Unit& u, const MmaCtx<D>& m, MmaState& st,
                                                     const Abort& ab) {
   using C = Cfg<D>;
-  const int J0 = union_begin(jb, je), J1 = union_end(jb, je);
+  const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
   if (J0 >= J1) return true;
-  auto active = [&](int t, int j) { return jb[t] <= j && j < je[t]; };
-  if (!m.wait_kv(0, ab)) return false;
+  auto active = [&](int t, int j) { return u.jb[t] <= j && j < u.je[t]; };
+  const int r0 = st.ring;
+  if (!m.wait_kv(r0, ab)) return false;
   tc_fence_after();
 #pragma unroll
-  for (int t = 0; t < kTiles; ++t) {
-    if (active(t, J0)) {
-      m.issue_s(t, 0);
-      m.commit(C::kSFull + t);
-    }
-  }
-  m.commit(C::kKVEmpty + 0);  // K_{J0} (slot 0) is free once the S(J0) are done
+  for (int t = 0; t < kTiles; ++t)
+    if (active(t, J0) && !issue_s_step<D>(t, r0 % C::kSlots, J0 == u.je[t] - 1, m, st, ab)) return false;
+  m.commit(C::kKVEmpty + r0 % C::kSlots);  // K_{J0} is free once the S(J0) are done
   for (int j = J0; j < J1; ++j) {
     if (j + 1 < J1) {
-      const int kidx = 2 * (j + 1 - J0);
+      const int kidx = r0 + 2 * (j + 1 - J0);
       if (!m.wait_kv(kidx, ab)) return false;
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t) {
-        if (active(t, j + 1)) {
-          if (j + 1 > jb[t]) {  // S_t(j) must have been read first
-            if (!m.wait(C::kSFree + t, j - jb[t], ab)) return false;
-            tc_fence_after();
-          }
-          m.issue_s(t, kidx % C::kSlots);
-          m.commit(C::kSFull + t);
-        }
-      }
+      for (int t = 0; t < kTiles; ++t)
+        if (active(t, j + 1) && !issue_s_step<D>(t, kidx % C::kSlots, j + 1 == u.je[t] - 1, m, st, ab)) return false;
       m.commit(C::kKVEmpty + kidx % C::kSlots);
     }
-    const int vidx = 2 * (j - J0) + 1;
+    const int vidx = r0 + 2 * (j - J0) + 1;
     if (!m.wait_kv(vidx, ab)) return false;
 #pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-      if (active(t, j)) {
-        if (!m.wait(C::kPFull + t, j - jb[t], ab)) return false;
-        tc_fence_after();
-        m.issue_pv(t, vidx % C::kSlots, j == jb[t]);
-        m.commit(C::kPVDone + t);
-        if (j == je[t] - 1) m.commit(C::kOFull + t);
-      }
-    }
+    for (int t = 0; t < kTiles; ++t)
+      if (active(t, j) && !issue_pv_step<D>(t, vidx % C::kSlots, j == u.jb[t], j == u.je[t] - 1, m, st, ab))
+        return false;
     m.commit(C::kKVEmpty + vidx % C::kSlots);
   }
+  st.ring = r0 + 2 * (J1 - J0);
   return true;
 }
 
 // P aliased over S (d = 128): S_t(j+1) is issued after P_t(j) V_j, which reads P_t from the same
 // columns (tcgen05.mma operations of one CTA execute in issue order).
 template <int D>
-__device__ __forceinline__ bool mma_loop_aliased_p(const int (&jb)[2], const int (&je)[2], const MmaCtx<D>& m,
+__device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D>& m, MmaState& st,
                                                    const Abort& ab) {
   using C = Cfg<D>;
-  const int J0 = union_begin(jb, je), J1 = union_end(jb, je);
+  const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
   if (J0 >= J1) return true;
-  auto active = [&](int t, int j) { return jb[t] <= j && j < je[t]; };
+  auto active = [&](int t, int j) { return u.jb[t] <= j && j < u.je[t]; };
+  const int r0 = st.ring;
   for (int j = J0; j <= J1; ++j) {
-    const int r = j - J0;  // ring step
-    if (j < J1 && !m.wait_kv(2 * r, ab)) return false;
-    if (j > J0 && !m.wait_kv(2 * (r - 1) + 1, ab)) return false;
+    const int r = r0 + 2 * (j - J0);  // ring index of K_j
+    if (j < J1 && !m.wait_kv(r, ab)) return false;
+    if (j > J0 && !m.wait_kv(r - 1, ab)) return false;  // V_{j-1}
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-      if (j > J0 && active(t, j - 1)) {
-        if (!m.wait(C::kPFull + t, j - 1 - jb[t], ab)) return false;
-        tc_fence_after();
-        m.issue_pv(t, (2 * (r - 1) + 1) % C::kSlots, j - 1 == jb[t]);
-        if (j - 1 == je[t] - 1) m.commit(C::kOFull + t);
-      }
-      if (j < J1 && active(t, j)) {
-        m.issue_s(t, (2 * r) % C::kSlots);
-        m.commit(C::kSFull + t);
-      }
+      if (j > J0 && active(t, j - 1) &&
+          !issue_pv_step<D>(t, (r - 1) % C::kSlots, j - 1 == u.jb[t], j - 1 == u.je[t] - 1, m, st, ab))
+        return false;
+      if (j < J1 && active(t, j) && !issue_s_step<D>(t, r % C::kSlots, j == u.je[t] - 1, m, st, ab)) return false;
     }
-    if (j < J1) m.commit(C::kKVEmpty + (2 * r) % C::kSlots);
-    if (j > J0) m.commit(C::kKVEmpty + (2 * (r - 1) + 1) % C::kSlots);
+    if (j < J1) m.commit(C::kKVEmpty + r % C::kSlots);
+    if (j > J0) m.commit(C::kKVEmpty + (r - 1) % C::kSlots);
   }
+  st.ring = r0 + 2 * (J1 - J0);
   return true;
 }
 
 // Whole warp.
 template <int D>
-__device__ __forceinline__ void mma_role(const int (&jb)[2], const int (&je)[2], uint32_t tmem, uint32_t sbase,
-                                         const Abort& ab) {
+__device__ __forceinline__ void mma_role(uint32_t tmem, uint32_t sbase, const Args& a, Abort ab) {
   using C = Cfg<D>;
   MmaCtx<D> m;
   m.init(tmem, sbase);
+  MmaState st;
   bool ok = true;
+  Unit u;
+  for (int k = 0; ok && cta_unit(k, a, u); ++k) {
+    ab.renew(a.timeout_ns);
 #pragma unroll
-  for (int t = 0; t < kTiles; ++t)
-    if (je[t] > jb[t] && ok) ok = m.wait(C::kQFull + t, 0, ab);
-  if (ok) ok = C::kSepP ? mma_loop_separate_p<D>(jb, je, m, ab) : mma_loop_aliased_p<D>(jb, je, m, ab);
+    for (int t = 0; t < kTiles; ++t)
+      if (u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
+    if (ok) ok = C::kSepP ? mma_unit_separate_p<D>(u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
+  }
   // Before the CTA winds down, every MMA (and every arrival its commits make on this CTA's
   // barriers) has completed, on the normal path and after a timeout alike.
   m.commit(C::kDrain);
@@ -598,14 +691,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5;
 
-  // Heaviest causal work first: the last query blocks of every head are launched first.
-  const int unit = a.units_per_head - 1 - static_cast<int>(blockIdx.x) / a.BH;
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
-  const int row0 = unit * kTiles * kBlockM;
-  int jb[2], je[2];
-  key_tiles(row0, a, jb[0], je[0]);
-  key_tiles(row0 + kBlockM, a, jb[1], je[1]);
-
   if (threadIdx.x == 0) {
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(sbar + 8 * (C::kQFull + t), 1);
@@ -614,6 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sbar + 8 * (C::kPFull + t), kBlockM / 32);
       mbar_init(sbar + 8 * (C::kPVDone + t), 1);
       mbar_init(sbar + 8 * (C::kOFull + t), 1);
+      mbar_init(sbar + 8 * (C::kQFree + t), 1);
+      mbar_init(sbar + 8 * (C::kOFree + t), kBlockM / 32);  // one arrival per softmax warp
     }
     mbar_init(sbar + 8 * C::kDrain, 1);
     for (int s = 0; s < C::kSlots; ++s) {
@@ -634,13 +721,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   Abort ab{abort_flag, a.status, globaltimer_ns() + a.timeout_ns};
 
   if (warp < 8) {
-    const int t = warp >> 2;
-    softmax_role<D>(t, jb[t], je[t] - jb[t], row0, bh, tmem, sbar, a, ab);
+    softmax_role<D>(warp >> 2, tmem, sbar, a, ab);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, jb, je, row0, bh, sbase, a.drop_kv_block, ab);
+    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, sbase, a, ab);
     __syncwarp();
   } else {
-    mma_role<D>(jb, je, tmem, sbase, ab);
+    mma_role<D>(tmem, sbase, a, ab);
   }
 
   tc_fence_before();
@@ -676,11 +762,21 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.wr = p.window_right;
   a.off = p.Nk - p.Nq;
   a.units_per_head = (p.Nq + kTiles * kBlockM - 1) / (kTiles * kBlockM);
+  a.total_units = a.units_per_head * a.BH;
   a.c_log2 = p.scale * 1.4426950408889634f;
   a.status = status;
   a.timeout_ns = timeout_ns;
   a.drop_kv_block = p.drop_kv_block;
-  const unsigned int grid = static_cast<unsigned int>(a.units_per_head) * static_cast<unsigned int>(a.BH);
+  // Persistent: one CTA per SM (each holds all of an SM's tensor memory), looping over the units.
+  static int sm_count[64] = {};
+  if (dev < 0 || dev >= 64 || sm_count[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) sm_count[dev] = n;
+    else return cudaErrorInvalidDevice;
+  }
+  const unsigned int grid = static_cast<unsigned int>(min(a.total_units, sm_count[dev]));
   prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
