@@ -41,6 +41,16 @@ int test_drop_kv_block() {
   return j;
 }
 
+// Failure-detection testing only: FATTN_TEST_DROP_BWD_KV=1 makes the backward kernel skip its key
+// and value loads, so that its bounded waits give up and report FATTN_ERR_TIMEOUT.
+int test_drop_bwd_kv() {
+  static int on = [] {
+    const char* s = getenv("FATTN_TEST_DROP_BWD_KV");
+    return s ? atoi(s) : 0;
+  }();
+  return on;
+}
+
 // Device address of g_device_status for the current device, looked up once per device.
 cudaError_t device_status_ptr(unsigned int** out) {
   static std::mutex mu;
@@ -191,7 +201,8 @@ fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
-  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, wl, wr, scale, ws_dq, ws_ext_q, ws_ext_do};
+  BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, wl, wr, scale, ws_dq, ws_ext_q, ws_ext_do,
+               test_drop_bwd_kv()};
   if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;

@@ -58,6 +58,9 @@ struct BwdProblem {
   float* ws_dq;    // [B*H][Nq_pad][d] fp32 dQ accumulator
   void* ws_ext_q;   // [B*H][Nq_pad][16] bf16: three terms of -L / scale (per query row)
   void* ws_ext_do;  // [B*H][Nq_pad][16] bf16: three terms of -D
+  // Failure-detection testing only (never set in normal use): the key and value tiles are not
+  // loaded, so the kernel's waits for them must give up and report a timeout.
+  int drop_kv;
 };
 
 // Query rows of the backward workspace per head: Nq rounded up to the 128-row query tile.

@@ -1,10 +1,11 @@
 """Failure detection without a GPU fault.
 
-Every wait in the prefill kernel is bounded.  A wait that gives up sets the library's device
+Every wait in the prefill and backward kernels is bounded.  A wait that gives up sets the library's device
 status word, and the kernel then winds down: in-flight copies land, MMAs drain, TMEM is freed.
 The host reads the word with fattn_last_error.  The test makes one wait run out: a test-only switch
 (FATTN_TEST_DROP_KV_BLOCK) stops the producer from loading one key tile, so nothing ever completes
-that tile's barrier.  The test then checks that the call returns, that the timeout is reported
+that tile's barrier (FATTN_TEST_DROP_BWD_KV does the same for the backward's key and value
+tiles).  The test then checks that the call returns, that the timeout is reported
 exactly once, and that the context is still usable.  It runs in a child process because the
 switches are read once per process.
 """
@@ -42,6 +43,44 @@ compare(od, ld, o_ref, l_ref, what="decode after a reported timeout")
 assert fa.fattn_last_error() == fa.FATTN_OK
 print("FAILURE-DETECTION-OK")
 """
+
+
+CHILD_BWD = r"""
+import math, sys
+sys.path.insert(0, sys.argv[1])
+sys.path.insert(0, sys.argv[1] + "/tests")
+import torch
+import exact_attention_31_gb300 as fa
+from exact_attention_31_gb300.workloads import make_dout, make_qkv
+from parity_utils import compare, oracle_full
+
+q, k, v, _ = make_qkv(1, 2, 512, 512, 64, seed=9, device="cuda")
+do = make_dout(1, 2, 512, 64, seed=9, device="cuda")
+o, lse = fa.fattn_fwd(q, k, v, causal=True)        # the forward is untouched by the switch
+torch.cuda.synchronize()
+assert fa.fattn_last_error() == fa.FATTN_OK
+fa.fattn_bwd(q, k, v, o, lse, do, causal=True)     # no key/value tile is ever loaded
+torch.cuda.synchronize()
+assert fa.fattn_last_error() == fa.FATTN_ERR_TIMEOUT
+assert fa.fattn_last_error() == fa.FATTN_OK
+
+o2, l2 = fa.fattn_fwd(q, k, v, causal=True)
+torch.cuda.synchronize()
+o_ref, l_ref = oracle_full(q, k, v, True, 1 / math.sqrt(64))
+compare(o2, l2, o_ref, l_ref, what="forward after a reported backward timeout")
+assert fa.fattn_last_error() == fa.FATTN_OK
+print("FAILURE-DETECTION-BWD-OK")
+"""
+
+
+@pytest.mark.gpu
+def test_backward_bounded_wait_reports_timeout_and_context_survives():
+    env = dict(os.environ, FATTN_WAIT_TIMEOUT_MS="200", FATTN_TEST_DROP_BWD_KV="1")
+    env.pop("FATTN_TEST_DROP_KV_BLOCK", None)
+    r = subprocess.run([sys.executable, "-c", CHILD_BWD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "FAILURE-DETECTION-BWD-OK" in r.stdout
 
 
 @pytest.mark.gpu
