@@ -79,8 +79,8 @@ template <int D>
 struct BCfg {
   static constexpr bool kTwoS = (D == 64);
   static constexpr int kSBufs = kTwoS ? 2 : 1;
-  static constexpr int kStages = kTwoS ? 2 : 1;   // Q_i/dO_i buffers
-  static constexpr int kDSBufs = kTwoS ? 2 : 1;   // dS^T buffers
+  static constexpr int kStages = kTwoS ? 3 : 1;   // Q_i/dO_i buffers
+  static constexpr int kDSBufs = 1;               // dS^T buffers
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kTile = kBM * D * 2;  // one 128-row bf16 tile of Q, K, V or dO
   static constexpr uint32_t kKOff = 0;
@@ -465,15 +465,15 @@ __device__ __forceinline__ bool mma_schedule_two(int n, const BMma<D>& m, const 
     }
     if (!m.wait(C::kCDone, i, ab)) return false;
     tc_fence_after();
-    // dV_i, dK_i, dQ_i: the dO and Q stages are released as early as possible (measured against
-    // issuing dQ_i first, which empties its columns for S^T of tile i+2 sooner: 2 % slower).
-    m.issue_dv(b, st, i == 0);
-    m.commit(C::kOEmpty + st);
+    // dK_i and dQ_i first: they release the one dS^T buffer, which the compute warps of tile i+1
+    // are about to refill; then dV_i.  (Measured: 2 % faster than dV, dK, dQ with three Q/dO stages.)
     m.issue_dk(dsb, st, i == 0);
     m.commit(C::kQEmpty + st);
     m.issue_dq(b, dsb);
     m.commit(C::kDQFull + b);
     m.commit(C::kDSEmpty + dsb);
+    m.issue_dv(b, st, i == 0);
+    m.commit(C::kOEmpty + st);
   }
   m.commit(C::kAccDone);
   return true;
