@@ -22,6 +22,7 @@ __all__ = [
     "fattn_bwd_workspace_size",
     "fattn_fwd_masked",
     "fattn_decode",
+    "fattn_decode_masked",
     "fattn_decode_static",
     "fattn_decode_num_splits",
     "fattn_decode_workspace_size",
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
     L.fattn_decode_workspace_size.restype = sz
     L.fattn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     L.fattn_decode.restype = i
+    L.fattn_decode_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    L.fattn_decode_masked.restype = i
     L.fattn_decode_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     L.fattn_decode_static.restype = i
     L.fattn_last_error.argtypes = [vp]
@@ -213,12 +216,13 @@ def fattn_decode_workspace_size(B: int, H: int, Nk: int, d: int, num_splits: int
 
 
 def fattn_decode(q, k_cache, v_cache, scale: float | None = None, num_splits: int = 0, workspace=None,
-                 out=None, lse=None, stream=None, want_lse: bool = True):
+                 out=None, lse=None, stream=None, want_lse: bool = True, window=None):
     """One query token per (b, h) against a KV cache, split-KV + combine on the GPU.
 
     q: bf16 [B,H,1,d]; k_cache, v_cache: bf16 [B,H,Nk,d].  ``workspace`` is a CUDA uint8 tensor of
     at least fattn_decode_workspace_size(...) bytes (allocated here if omitted).
-    Returns (out bf16 [B,H,1,d], lse fp32 [B,H,1] or None).
+    ``window=(window_left, window_right)`` restricts the query to the last window_left + 1 keys
+    (fattn_decode_masked).  Returns (out bf16 [B,H,1,d], lse fp32 [B,H,1] or None).
     """
     import torch
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
@@ -242,6 +246,15 @@ def fattn_decode(q, k_cache, v_cache, scale: float | None = None, num_splits: in
         lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
     if lse is not None:
         _check(lse, "lse", torch.float32)
+    if window is not None:
+        st = lib().fattn_decode_masked(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                       lse.data_ptr() if lse is not None else None, B, H, Nk, d, int(window[0]),
+                                       int(window[1]), float(scale), int(num_splits), workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream_handle(stream, q.device))
+        if st != FATTN_OK:
+            raise FattnError(st, "fattn_decode_masked")
+        return out, lse
     st = lib().fattn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
                             lse.data_ptr() if lse is not None else None, B, H, Nk, d, float(scale),
                             int(num_splits), workspace.data_ptr(),

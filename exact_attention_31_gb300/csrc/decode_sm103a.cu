@@ -63,16 +63,17 @@ template <int D>
 __global__ void __launch_bounds__(kSplitWarps * 32)
     decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                         const __nv_bfloat16* __restrict__ v, float* __restrict__ ws_o,
-                        float* __restrict__ ws_ml, int BH, int Nk, int nblk, int S, float c_log2) {
+                        float* __restrict__ ws_ml, int BH, int Nk, int key_lo, int nblk, int S, float c_log2) {
   using C = SplitCfg<D>;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kSplitWarps + (threadIdx.x >> 5);
   if (gw >= BH * S) return;
   const int bh = gw / S;
   const int s = gw - bh * S;
-  const int key_begin = static_cast<int>((static_cast<long long>(s) * nblk / S) * kDecodeBlockKeys);
+  // split s covers 64-key blocks [s*nblk/S, (s+1)*nblk/S) of the visible keys [key_lo, Nk)
+  const int key_begin = key_lo + static_cast<int>((static_cast<long long>(s) * nblk / S) * kDecodeBlockKeys);
   const int key_end =
-      min(Nk, static_cast<int>((static_cast<long long>(s + 1) * nblk / S) * kDecodeBlockKeys));
+      min(Nk, key_lo + static_cast<int>((static_cast<long long>(s + 1) * nblk / S) * kDecodeBlockKeys));
   const int chunk = lane % C::kLanesPerRow;
   const int sub = lane / C::kLanesPerRow;
 
@@ -232,12 +233,12 @@ __global__ void __launch_bounds__(kCombineThreads)
 template <int D>
 cudaError_t launch_decode_d(const DecodeProblem& p, cudaStream_t stream) {
   const int BH = p.B * p.H;
-  const int nblk = (p.Nk + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
+  const int nblk = (p.Nk - p.key_lo + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
   const long long warps = static_cast<long long>(BH) * p.num_splits;
   const unsigned int grid = static_cast<unsigned int>((warps + kSplitWarps - 1) / kSplitWarps);
   decode_split_kernel<D><<<grid, kSplitWarps * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
-      static_cast<const __nv_bfloat16*>(p.v), p.ws_o, p.ws_ml, BH, p.Nk, nblk, p.num_splits,
+      static_cast<const __nv_bfloat16*>(p.v), p.ws_o, p.ws_ml, BH, p.Nk, p.key_lo, nblk, p.num_splits,
       p.scale * 1.4426950408889634f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

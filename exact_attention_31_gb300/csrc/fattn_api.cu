@@ -265,6 +265,35 @@ size_t fattn_decode_workspace_size(int B, int H, int Nk, int d, int num_splits) 
   return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256);
 }
 
+fattn_status fattn_decode_masked(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                 int B, int H, int Nk, int d, int window_left, int window_right, float scale,
+                                 int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (window_left < -1 || window_right < -1) return FATTN_ERR_INVALID_ARG;
+  if (Nk < 1) return FATTN_ERR_INVALID_ARG;
+  // The one query sits at position Nk - 1 (bottom-right): it sees keys [Nk - 1 - window_left, Nk - 1];
+  // window_right cannot exclude anything, and the last key is always visible.
+  const int key_lo = window_left >= 0 && window_left < Nk - 1 ? Nk - 1 - window_left : 0;
+  if (!q || !k_cache || !v_cache || !o || !workspace) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(workspace) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nk, 1)) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const int S = fattn_decode_num_splits(Nk - key_lo, num_splits);
+  if (S < 1) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * S > 0x7fffffffLL) return FATTN_ERR_INVALID_ARG;
+  const size_t need = fattn_decode_workspace_size(B, H, Nk - key_lo, d, num_splits);
+  if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+  const size_t parts = static_cast<size_t>(B) * H * S;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align_up(parts * d * sizeof(float), 256));
+  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, key_lo};
+  if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
 fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                           int B, int H, int Nk, int d, float scale, int num_splits, void* workspace,
                           size_t workspace_bytes, void* stream) {
@@ -284,7 +313,7 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
   float* ws_o = static_cast<float*>(workspace);
   float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                           align_up(parts * d * sizeof(float), 256));
-  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml};
+  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, 0};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
   return FATTN_OK;
 }
@@ -354,7 +383,7 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
   const size_t parts = static_cast<size_t>(B) * H * S;
   float* ws_o = static_cast<float*>(ws);
   float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(parts * d * sizeof(float), 256));
-  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml};
+  DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, 0};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
   return FATTN_OK;
 }

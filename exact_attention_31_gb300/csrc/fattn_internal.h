@@ -40,6 +40,7 @@ struct DecodeProblem {
   int num_splits;    // resolved, in [1, nblk]
   float* ws_o;       // [B*H*num_splits, d] partial unnormalised outputs
   float* ws_ml;      // [B*H*num_splits, 2] partial (m, l), m in log2 units of the scaled score
+  int key_lo;        // first visible key (a sliding window keeps keys [key_lo, Nk)); 0 = all
 };
 
 struct BwdProblem {

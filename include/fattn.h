@@ -162,6 +162,19 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
                           size_t workspace_bytes, void* stream);
 
 /*
+ * fattn_decode_masked -- fattn_decode under the banded masks of fattn_fwd_masked.  The one query of
+ * each (b, h) sits at position Nk - 1 (bottom-right alignment), so it sees the keys
+ * [Nk - 1 - window_left, Nk - 1] (all of them for window_left = -1 or >= Nk - 1); window_right
+ * cannot exclude a key and only has to be >= -1.  This is the decode step of a sliding-window model:
+ * window (W - 1, 0) attends to the last W cached keys.  num_splits and its 64-key blocks count
+ * the visible keys; the workspace needs fattn_decode_workspace_size(B, H, W_visible, d, num_splits)
+ * bytes, which the size for all Nk keys always covers.  Other arguments as for fattn_decode.
+ */
+fattn_status fattn_decode_masked(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                 int B, int H, int Nk, int d, int window_left, int window_right, float scale,
+                                 int num_splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fattn_decode_static -- fattn_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point: it exists for users of this library who are
