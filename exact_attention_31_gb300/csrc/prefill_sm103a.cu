@@ -30,9 +30,9 @@
 // reference is only raised when the tile max exceeds it by more than kRescaleLog2 (the rescale is
 // exact for any reference as long as l, O and L use the same one: exp(a-c) = exp(a-b) exp(b-c),
 // "FlashAttention: attention was never compute-bound", On the maths anxiety), which keeps most
-// tiles from touching O in TMEM at all.  Two row sums are kept: l from the fp32 weights, which
-// gives L = m + log(l), and lr from the bf16-rounded weights that enter P V, which normalises O so
-// that its numerator and denominator see the same weights.  The per-row arithmetic uses packed
+// tiles from touching O in TMEM at all.  One row sum l of the fp32 weights gives both O / l and
+// L = m + log(l); P V sees the weights rounded to bf16, so O carries a relative bias of at most
+// 2^-9 (one rounding of the dominant weight) on rows with one dominant key.  The per-row arithmetic uses packed
 // fp32x2 FMA/add and three-input max with several independent accumulators, so one thread's row
 // is not a single long dependency chain.
 #include <cuda_bf16.h>
@@ -213,14 +213,6 @@ __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) 
       : "f"(b0), "f"(b1));
 }
 
-// a0 += low bf16 of pk, a1 += high bf16 of pk (mixed-precision adds, exact widening)
-__device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t pk) {
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "r"(pk));
-}
-
 // ------------------------------------------------------------------------------------------------
 // Softmax group: one thread per query row.
 // ------------------------------------------------------------------------------------------------
@@ -245,8 +237,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   const float c = a.c_log2;
 
   float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
-  float l = 0.f;            // sum of the fp32 weights: L = m + log(l)
-  float lr = 0.f;           // sum of the bf16-rounded weights that entered P V: O = O / lr
+  float l = 0.f;            // sum of the fp32 weights: O = O / l, L = m + log(l)
   bool ok = true;
   for (int step = 0; step < n_tiles; ++step, ++g) {
     const int j = jb + step;
@@ -295,13 +286,11 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
       corr = ex2_approx(m_ref - m_new);  // 0 on the first tile
       m_ref = m_new;
       l *= corr;
-      lr *= corr;
     }
     const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
     uint32_t p[2][32];
     float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of fp32 partial sums
-    float lrs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
 #pragma unroll
@@ -314,11 +303,9 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
         p[h >> 1][(h & 1) * 16 + i] = pk;
         const int acc = (i & 1) * 2;
         fadd2(ls[acc], ls[acc + 1], e0, e1);
-        add_bf16x2(lrs[acc], lrs[acc + 1], pk);
       }
     }
     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-    lr += (lrs[0] + lrs[1]) + (lrs[2] + lrs[3]);
 
     if constexpr (C::kSepP) {
       // P_t is still read by the previous P_t V until it completes.
@@ -371,8 +358,8 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
 
   if (!warp_wait(sbar + 8 * (C::kOFull + t), done & 1, ab)) return false;
   tc_fence_after();
-  // A row that saw no key has l = lr = 0 and m = -inf: o = 0 and L = -inf.
-  const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+  // A row that saw no key has l = 0 and m = -inf: o = 0 and L = -inf.
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int h = 0; h < D / 32; ++h) {
     uint32_t o[32];
