@@ -289,8 +289,10 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     }
     const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-    uint32_t p[2][32];
+    // P in two halves of 64 keys, each stored to TMEM as soon as it is packed.
+    uint32_t ph[32];
     float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of fp32 partial sums
+    bool pv_ok = true;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
 #pragma unroll
@@ -299,26 +301,25 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
         ffma2_bc(x0, x1, __uint_as_float(s[h][2 * i]), __uint_as_float(s[h][2 * i + 1]), c, neg_m);
         const float e0 = ex2_approx(x0);
         const float e1 = ex2_approx(x1);
-        const uint32_t pk = pack_bf16x2(e0, e1);
-        p[h >> 1][(h & 1) * 16 + i] = pk;
+        ph[(h & 1) * 16 + i] = pack_bf16x2(e0, e1);
         const int acc = (i & 1) * 2;
         fadd2(ls[acc], ls[acc + 1], e0, e1);
       }
-    }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-
-    if constexpr (C::kSepP) {
-      // P_t is still read by the previous P_t V until it completes.
-      if (g > 0) {
-        if (!warp_wait(sbar + 8 * (C::kPVDone + t), (g - 1) & 1, ab)) {
-          ok = false;
-          break;
+      if (h & 1) {
+        if (C::kSepP && h == 1 && g > 0) {
+          // P_t is still read by the previous P_t V until it completes.
+          pv_ok = warp_wait(sbar + 8 * (C::kPVDone + t), (g - 1) & 1, ab);
+          if (!pv_ok) break;
+          tc_fence_after();
         }
-        tc_fence_after();
+        tmem_st_32x32b_x32(tP + 32 * (h >> 1), ph);
       }
     }
-    tmem_st_32x32b_x32(tP, p[0]);
-    tmem_st_32x32b_x32(tP + 32, p[1]);
+    if (!pv_ok) {
+      ok = false;
+      break;
+    }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
     // Rescale O_t (last written by P_t(j-1) V_{j-1}, now complete) when the reference moved.
     if (step > 0 && __any_sync(0xffffffffu, need)) {
