@@ -12,11 +12,15 @@
 // and computed while the current unit finishes; two barriers guard the hand-over (the last S_t has
 // read Q_t before Q_t is reloaded; the epilogue has read O_t before the next P_t V overwrites it).
 //
-// How it maps onto one SM (one CTA per SM, 320 threads):
+// How it maps onto one SM (one CTA per SM, 352 threads):
 //   warps 0-3  softmax group for query tile 0 (one thread per query row / TMEM lane)
 //   warps 4-7  softmax group for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_j, V_j through a ring of shared-memory slots
-//   warp  9    MMA issuer (one thread) and TMEM owner
+//   warp  9    MMA issuer and TMEM owner; with d = 64 it issues query tile 0's products only
+//   warp  10   (d = 64) MMA issuer of query tile 1's products
+// With d = 64 each query tile has an MMA warp of its own, so one tile's next S never waits in the
+// issue order behind the other tile's P V; a key/value slot is released once both warps' products
+// that read it have completed.
 // Tensor memory (512 columns x 128 lanes, fp32): S_t at columns 128t and O_t at 256 + 128t.  The
 // bf16 probabilities P_t are fed to the second MMA straight from TMEM.  With d = 64, O_t uses only
 // half of its 128 columns and P_t gets the other half, so S_t(j+1) = Q_t K_{j+1}^T can be issued
@@ -47,9 +51,10 @@ namespace {
 constexpr int kBlockM = 128;       // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;       // keys per key/value tile
 constexpr int kTiles = 2;          // query tiles per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;   // tile 0 (d = 64) or both tiles (d = 128); TMEM owner
+constexpr int kMmaWarp1 = 10; // tile 1 (d = 64)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtomBytes = kBlockM * 128;  // one 128-row x 128-byte swizzled chunk
@@ -72,10 +77,12 @@ struct Cfg {
   static constexpr int kOFull = 10;             // [2] last P V of tile t done
   static constexpr int kQFree = 12;             // [2] the unit's last S_t has read Q_t
   static constexpr int kOFree = 14;             // [2] O_t read out by the epilogue (one arrival per warp)
-  static constexpr int kDrain = 16;             // [1] wind-down after a timeout
+  static constexpr int kDrain = 16;             // [1] wind-down of MMA warp 9
   static constexpr int kKVFull = 17;            // [kSlots]
   static constexpr int kKVEmpty = 17 + kSlots;  // [kSlots]
-  static constexpr int kNumBars = 17 + 2 * kSlots;
+  static constexpr int kDrain1 = 17 + 2 * kSlots;  // [1] wind-down of MMA warp 10
+  static constexpr int kNumBars = 18 + 2 * kSlots;
+  static constexpr int kMmaWarps = kSepP ? 2 : 1;   // commits that release a K/V slot
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
   // tensor-memory columns
@@ -574,37 +581,35 @@ __device__ __forceinline__ bool issue_pv_step(int t, int slot, bool first, bool 
   return true;
 }
 
-// Separate P (d = 64): S_t(j+1) is issued once S_t(j) has been read, P_t(j) V_j once P_t(j) is written.
-// Tile t visits key tiles [jb_t, je_t); ring index of K_j is ring + 2 (j - J0), of V_j one more.
+// Separate P (d = 64), one warp per query tile t: S_t(j+1) is issued once S_t(j) has been read,
+// P_t(j) V_j once P_t(j) is written.  The warp waits for every K/V tile of the unit's union range
+// and commits once per tile to its slot's K/V-empty barrier (two arrivals release a slot), whether
+// or not tile t uses it; a commit for a slot's next use can only follow that use's load, which
+// itself waited for both of the previous use's arrivals.  Ring index of K_j is ring + 2 (j - J0),
+// of V_j one more.
 template <int D>
-__device__ __forceinline__ bool mma_unit_separate_p(const Unit& u, const MmaCtx<D>& m, MmaState& st,
-                                                    const Abort& ab) {
+__device__ __forceinline__ bool mma_unit_tile(int t, const Unit& u, const MmaCtx<D>& m, MmaState& st,
+                                              const Abort& ab) {
   using C = Cfg<D>;
   const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
   if (J0 >= J1) return true;
-  auto active = [&](int t, int j) { return u.jb[t] <= j && j < u.je[t]; };
+  const int jb = t ? u.jb[1] : u.jb[0], je = t ? u.je[1] : u.je[0];
   const int r0 = st.ring;
   if (!m.wait_kv(r0, ab)) return false;
   tc_fence_after();
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t)
-    if (active(t, J0) && !issue_s_step<D>(t, r0 % C::kSlots, J0 == u.je[t] - 1, m, st, ab)) return false;
-  m.commit(C::kKVEmpty + r0 % C::kSlots);  // K_{J0} is free once the S(J0) are done
+  if (jb <= J0 && J0 < je && !issue_s_step<D>(t, r0 % C::kSlots, J0 == je - 1, m, st, ab)) return false;
+  m.commit(C::kKVEmpty + r0 % C::kSlots);  // K_{J0} is free once S_t(J0) is done
   for (int j = J0; j < J1; ++j) {
     if (j + 1 < J1) {
       const int kidx = r0 + 2 * (j + 1 - J0);
       if (!m.wait_kv(kidx, ab)) return false;
-#pragma unroll
-      for (int t = 0; t < kTiles; ++t)
-        if (active(t, j + 1) && !issue_s_step<D>(t, kidx % C::kSlots, j + 1 == u.je[t] - 1, m, st, ab)) return false;
+      if (jb <= j + 1 && j + 1 < je && !issue_s_step<D>(t, kidx % C::kSlots, j + 1 == je - 1, m, st, ab))
+        return false;
       m.commit(C::kKVEmpty + kidx % C::kSlots);
     }
     const int vidx = r0 + 2 * (j - J0) + 1;
     if (!m.wait_kv(vidx, ab)) return false;
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t)
-      if (active(t, j) && !issue_pv_step<D>(t, vidx % C::kSlots, j == u.jb[t], j == u.je[t] - 1, m, st, ab))
-        return false;
+    if (jb <= j && j < je && !issue_pv_step<D>(t, vidx % C::kSlots, j == jb, j == je - 1, m, st, ab)) return false;
     m.commit(C::kKVEmpty + vidx % C::kSlots);
   }
   st.ring = r0 + 2 * (J1 - J0);
@@ -640,9 +645,10 @@ __device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D
   return true;
 }
 
-// Whole warp.
+// Whole warp.  `tt` is the query tile of this warp (d = 64); with d = 128 the one MMA warp (tt = 0)
+// issues both tiles' products.
 template <int D>
-__device__ __forceinline__ void mma_role(uint32_t tmem, uint32_t sbase, const Args& a, Abort ab) {
+__device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, const Args& a, Abort ab) {
   using C = Cfg<D>;
   MmaCtx<D> m;
   m.init(tmem, sbase);
@@ -653,15 +659,16 @@ __device__ __forceinline__ void mma_role(uint32_t tmem, uint32_t sbase, const Ar
     ab.renew(a.timeout_ns);
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
-      if (u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
-    if (ok) ok = C::kSepP ? mma_unit_separate_p<D>(u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
+      if ((!C::kSepP || t == tt) && u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
+    if (ok) ok = C::kSepP ? mma_unit_tile<D>(tt, u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
   }
   // Before the CTA winds down, every MMA (and every arrival its commits make on this CTA's
   // barriers) has completed, on the normal path and after a timeout alike.
-  m.commit(C::kDrain);
+  const int drain = tt ? C::kDrain1 : C::kDrain;
+  m.commit(drain);
   volatile uint32_t never = 0;
   const uint64_t until = ok ? ab.deadline : globaltimer_ns() + 50ull * 1000 * 1000;
-  mbar_wait_bounded(m.sbar + 8 * C::kDrain, 0, &never, until);
+  mbar_wait_bounded(m.sbar + 8 * drain, 0, &never, until);
   __syncwarp();
 }
 
@@ -691,9 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sbar + 8 * (C::kOFree + t), kBlockM / 32);  // one arrival per softmax warp
     }
     mbar_init(sbar + 8 * C::kDrain, 1);
+    mbar_init(sbar + 8 * C::kDrain1, 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(sbar + 8 * (C::kKVFull + s), 1);
-      mbar_init(sbar + 8 * (C::kKVEmpty + s), 1);
+      mbar_init(sbar + 8 * (C::kKVEmpty + s), C::kMmaWarps);
     }
     *abort_flag = 0u;
     fence_mbarrier_init();
@@ -713,8 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kProducerWarp) {
     if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, sbase, a, ab);
     __syncwarp();
-  } else {
-    mma_role<D>(tmem, sbase, a, ab);
+  } else if (warp == kMmaWarp) {
+    mma_role<D>(0, tmem, sbase, a, ab);
+  } else if (C::kSepP && warp == kMmaWarp1) {
+    mma_role<D>(1, tmem, sbase, a, ab);
   }
 
   tc_fence_before();
