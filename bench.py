@@ -229,15 +229,15 @@ def max_over_ranks(x, dist, device):
 # ------------------------------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline figure)
 # ------------------------------------------------------------------------------------------------
-def oracle_prefill_sample(q, k, v, budget_s, seed=0):
-    """Time the oracle on random query rows of the prefill workload until `budget_s` has passed.
-    Returns (flops_done, seconds, rows_done, threads)."""
+def oracle_prefill_sample(q, k, v, budget_s, seed=0, threads=None):
+    """Time the oracle on random query rows of the prefill workload until `budget_s` has passed,
+    on `threads` host threads (default: all).  Returns (flops_done, seconds, rows_done, threads)."""
     import numpy as np
     import oracle
     B, H, N, d = q.shape
     qq = q.reshape(B * H, N, d)
     rng = np.random.default_rng(seed)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     flops = 0.0
     rows_done = 0
     t_total = 0.0
@@ -290,7 +290,8 @@ def host_inputs_f64(seed_prefill=0xFA77E004, seed_decode_pairs=0xFA77E005):
 
 def cpu_baseline(budget_s=12.0):
     pf, df = host_inputs_f64()
-    flops, secs, rows, threads = oracle_prefill_sample(*pf, budget_s=budget_s * 0.75)
+    flops, secs, rows, threads = oracle_prefill_sample(*pf, budget_s=budget_s * 0.6)
+    flops1, secs1, rows1, _ = oracle_prefill_sample(*pf, budget_s=budget_s * 0.15, seed=2, threads=1)
     kvb, dsecs, pairs, _ = oracle_decode_sample(*df, budget_s=budget_s * 0.25)
     return {
         "value": flops / secs / 1e12,
@@ -300,6 +301,8 @@ def cpu_baseline(budget_s=12.0):
         "sample": (f"{rows} random query rows of the causal B1 H32 N8192 d64 prefill ({flops / 1e9:.2f} "
                    f"GFLOP in {secs:.1f} s); decode: {pairs} (b,h) pairs of Nk=16384 d=128"),
         "decode_gbs": kvb / dsecs / 1e9,
+        "value_1core": flops1 / secs1 / 1e12,
+        "sample_1core": f"{rows1} random query rows of the same prefill on one host thread ({secs1:.1f} s)",
     }
 
 
