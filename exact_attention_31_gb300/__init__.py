@@ -79,6 +79,14 @@ def lib() -> ctypes.CDLL:
     L.fattn_decode_masked.restype = i
     L.fattn_decode_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     L.fattn_decode_static.restype = i
+    L.fattn_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.fattn_fwd_host_workspace_size.restype = sz
+    L.fattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+    L.fattn_fwd_host.restype = i
+    L.fattn_decode_host_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.fattn_decode_host_workspace_size.restype = sz
+    L.fattn_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    L.fattn_decode_host.restype = i
     L.fattn_last_error.argtypes = [vp]
     L.fattn_last_error.restype = i
     L.fattn_status_string.argtypes = [i]
@@ -293,6 +301,112 @@ def fattn_decode_static(q, k_cache, v_cache, scale: float | None = None, num_spl
                                    float(scale), int(num_splits), _stream_handle(stream, q.device))
     if st != FATTN_OK:
         raise FattnError(st, "fattn_decode_static")
+    return out, lse
+
+
+def _check_host(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+
+
+def _band(causal, window):
+    if window is not None:
+        return int(window[0]), int(window[1])
+    return (-1, 0) if causal else (-1, -1)
+
+
+def fattn_fwd_host_workspace_size(B, H, Nq, Nk, d, heads_per_chunk: int = 0) -> int:
+    return lib().fattn_fwd_host_workspace_size(int(B), int(H), int(Nq), int(Nk), int(d), int(heads_per_chunk))
+
+
+def fattn_decode_host_workspace_size(B, H, Nk, d, window_left: int = -1, heads_per_chunk: int = 0) -> int:
+    return lib().fattn_decode_host_workspace_size(int(B), int(H), int(Nk), int(d), int(window_left),
+                                                  int(heads_per_chunk))
+
+
+def fattn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                   window=None, heads_per_chunk: int = 0, workspace=None, device=None, stream=None,
+                   want_lse: bool = True):
+    """fattn_fwd with q, k, v, out and lse in host memory (fattn_fwd_host): chunks of heads are copied
+    in, computed and copied back with the copies overlapping the kernels.  Pinned host tensors give
+    asynchronous copies.  ``workspace`` is a CUDA uint8 tensor of at least
+    fattn_fwd_host_workspace_size(...) bytes (allocated here if omitted).  Synchronise ``stream``
+    before reading out/lse.  Returns (out, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_host(t, n, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,H,Nq,d], k/v [B,H,Nk,d]")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q and k/v disagree on B, H or d")
+    Nk = k.shape[2]
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    _check_host(out, "out", torch.bfloat16)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=True)
+    if lse is not None:
+        _check_host(lse, "lse", torch.float32)
+    if workspace is None:
+        need = fattn_fwd_host_workspace_size(B, H, Nq, Nk, d, heads_per_chunk)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    _check(workspace, "workspace")
+    wl, wr = _band(causal, window)
+    st = lib().fattn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, wl, wr, float(scale),
+                              int(heads_per_chunk), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream, device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_fwd_host")
+    return out, lse
+
+
+def fattn_decode_host(q, k_cache, v_cache, scale: float | None = None, out=None, lse=None, window=None,
+                      heads_per_chunk: int = 0, workspace=None, device=None, stream=None, want_lse: bool = True):
+    """fattn_decode with q, the caches, out and lse in host memory (fattn_decode_host); with a
+    window only the visible keys are copied.  Synchronise ``stream`` before reading out/lse.
+    Returns (out, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_host(t, n, torch.bfloat16)
+    if q.dim() != 4 or q.shape[2] != 1 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected q [B,H,1,d] and k/v caches [B,H,Nk,d]")
+    B, H, _, d = q.shape
+    if k_cache.shape[0] != B or k_cache.shape[1] != H or k_cache.shape[3] != d:
+        raise ValueError("q and the caches disagree on B, H or d")
+    Nk = k_cache.shape[2]
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    _check_host(out, "out", torch.bfloat16)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, pin_memory=True)
+    if lse is not None:
+        _check_host(lse, "lse", torch.float32)
+    wl, wr = _band(False, window)
+    if workspace is None:
+        need = fattn_decode_host_workspace_size(B, H, Nk, d, wl, heads_per_chunk)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    _check(workspace, "workspace")
+    st = lib().fattn_decode_host(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, B, H, Nk, d, wl, wr, float(scale),
+                                 int(heads_per_chunk), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream_handle(stream, device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_decode_host")
     return out, lse
 
 

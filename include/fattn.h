@@ -206,6 +206,49 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
                                  void* stream);
 
 /*
+ * fattn_fwd_host / fattn_decode_host -- the same computations with the inputs and outputs in HOST
+ * memory.  The pages put the cost of attention in moving data between memory levels ("Flash
+ * Attention: The Hidden Gem", Background; "FlashAttention: attention was never compute-bound",
+ * The one formula); these entry points extend that to the host link: the (b, h) problems are cut
+ * into chunks of `heads_per_chunk` consecutive heads of the flattened [B * H] index, and chunk c + 1
+ * is copied to the device while chunk c is computed and chunk c - 1 is copied back, through two
+ * slots of a caller-owned device workspace.
+ *
+ *   q_host ... lse_host   host memory, same shapes and layouts as the device calls; lse_host may be
+ *                         NULL.  Page-locked memory (cudaHostAlloc / cudaHostRegister) lets the
+ *                         copies run asynchronously and overlap; pageable memory is accepted and
+ *                         gives the same results with less overlap.  No alignment is required.
+ *   window_left, window_right   the band of fattn_fwd_masked ((-1, 0) is causal, (-1, -1) none).
+ *                         For the decode only window_left matters (fattn_decode_masked): just the
+ *                         visible keys [Nk - 1 - window_left, Nk - 1] of each head are copied.
+ *   heads_per_chunk       0 picks a default (about four chunks for the forward, eight for the
+ *                         decode); otherwise 1 .. B * H.
+ *   workspace             device memory of at least the matching *_workspace_size bytes for the
+ *                         same arguments, 256-byte aligned, owned by the caller.
+ *   stream                the compute stream.  The copies run on two streams the library creates
+ *                         once per device and keeps for the life of the process, ordered against
+ *                         `stream` with events: the call's first copy waits for the work enqueued on
+ *                         `stream` before the call, and `stream` waits for the call's last copy.
+ *                         Synchronise `stream` before reading the host outputs.
+ *
+ * The kernels are those of the device calls, applied to each chunk as its own problem (B = 1,
+ * H = heads in the chunk), so the outputs equal the device calls' outputs for the same inputs.
+ * Calls that share a workspace, or that run from several host threads at once, must be serialised
+ * by the caller.  Returns the device calls' statuses, and FATTN_ERR_CUDA if a copy or an event call
+ * is refused.
+ */
+size_t fattn_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int heads_per_chunk);
+fattn_status fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                            float* lse_host, int B, int H, int Nq, int Nk, int d, int window_left,
+                            int window_right, float scale, int heads_per_chunk, void* workspace,
+                            size_t workspace_bytes, void* stream);
+size_t fattn_decode_host_workspace_size(int B, int H, int Nk, int d, int window_left, int heads_per_chunk);
+fattn_status fattn_decode_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                               float* lse_host, int B, int H, int Nk, int d, int window_left, int window_right,
+                               float scale, int heads_per_chunk, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
  * fattn_last_error -- wait for `stream`, then read and clear the library's on-device status word on
  * the current device.  Returns FATTN_OK, FATTN_ERR_TIMEOUT if some kernel's bounded wait gave up
  * since the last read (its outputs are then unspecified), or FATTN_ERR_CUDA if the stream reported

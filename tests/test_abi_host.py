@@ -150,3 +150,62 @@ def test_binding_fails_loudly_without_cuda_tensors():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fattn_fwd(q, q, q)
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,hpc,chunk", [(1, 32, 8192, 8192, 64, 0, 8), (2, 3, 100, 300, 128, 0, 2),
+                                                   (1, 5, 64, 64, 64, 2, 2), (1, 1, 1, 1, 64, 0, 1)])
+def test_fwd_host_workspace_size(L, B, H, Nq, Nk, d, hpc, chunk):
+    # two slots, each holding Q, K, V, O (bf16) and L (fp32) of `chunk` heads, every part 256-aligned;
+    # the default chunk is B*H/4 rounded up
+    slot = (_align256(chunk * Nq * d * 2) + 2 * _align256(chunk * Nk * d * 2) + _align256(chunk * Nq * d * 2)
+            + _align256(chunk * Nq * 4))
+    assert L.fattn_fwd_host_workspace_size(B, H, Nq, Nk, d, hpc) == 2 * slot
+
+
+def test_fwd_host_workspace_size_rejects(L):
+    assert L.fattn_fwd_host_workspace_size(1, 4, 8, 8, 96, 0) == 0     # d
+    assert L.fattn_fwd_host_workspace_size(1, 4, 8, 8, 64, 5) == 0     # more heads per chunk than heads
+    assert L.fattn_fwd_host_workspace_size(1, 4, 8, 8, 64, -1) == 0
+    assert L.fattn_fwd_host_workspace_size(0, 4, 8, 8, 64, 0) == 0
+
+
+def test_decode_host_workspace_size_copies_only_visible_keys(L):
+    # default chunk: B*H/8 rounded up; a window of the last 100 keys stages 100 keys per head
+    full = L.fattn_decode_host_workspace_size(2, 8, 4096, 128, -1, 0)
+    win = L.fattn_decode_host_workspace_size(2, 8, 4096, 128, 99, 0)
+    chunk = 2
+    kv_full, kv_win = 2 * _align256(chunk * 4096 * 128 * 2), 2 * _align256(chunk * 100 * 128 * 2)
+    assert full - win == 2 * (kv_full - kv_win) + 2 * (_align256(L.fattn_decode_workspace_size(1, chunk, 4096, 128, 0))
+                                                      - _align256(L.fattn_decode_workspace_size(1, chunk, 100, 128, 0)))
+    assert L.fattn_decode_host_workspace_size(2, 8, 4096, 128, 5000, 0) == full  # window wider than the cache
+    assert L.fattn_decode_host_workspace_size(2, 8, 4096, 128, -2, 0) == 0
+
+
+@pytest.mark.parametrize("change,expect", [
+    ({"q": None}, 1), ({"ws": A + 16}, 1), ({"ws_bytes": 1}, 1), ({"B": 0}, 1), ({"wl": -2}, 1),
+    ({"scale": float("nan")}, 1), ({"hpc": 9}, 1), ({"d": 80}, 2),
+])
+def test_fwd_host_rejects_bad_arguments(L, change, expect):
+    a = dict(q=A, k=A, v=A, o=A, lse=None, B=1, H=8, Nq=16, Nk=16, d=64, wl=-1, wr=0, scale=0.125, hpc=0,
+             ws=A, ws_bytes=1 << 30)
+    a.update(change)
+    st = L.fattn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                          a["wl"], a["wr"], a["scale"], a["hpc"], a["ws"], a["ws_bytes"], None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("change,expect", [
+    ({"o": None}, 1), ({"ws": A + 8}, 1), ({"ws_bytes": 1}, 1), ({"Nk": 0}, 1), ({"wr": -2}, 1),
+    ({"scale": -1.0}, 1), ({"hpc": -3}, 1), ({"d": 32}, 2),
+])
+def test_decode_host_rejects_bad_arguments(L, change, expect):
+    a = dict(q=A, k=A, v=A, o=A, lse=None, B=2, H=4, Nk=300, d=128, wl=-1, wr=-1, scale=0.1, hpc=0,
+             ws=A, ws_bytes=1 << 30)
+    a.update(change)
+    st = L.fattn_decode_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nk"], a["d"],
+                             a["wl"], a["wr"], a["scale"], a["hpc"], a["ws"], a["ws_bytes"], None)
+    assert st == expect
