@@ -479,6 +479,8 @@ def run_ours(args):
         # The step's dominant kernel by time is the decode's split kernel (about 78 % of the step in
         # the ncu launch list), so its roofline is the line's "roofline"; the prefill's sits beside it.
         line["roofline"] = rd
+    if args.configs and do_prefill and window is None and rank == 0:
+        line["configs_measured"] = measure_configs(fa, dev, stream, peaks)
     if args.cpu_budget > 0:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if e2e is not None:
@@ -590,6 +592,61 @@ def run_backward(args):
         "clocks": sampler.summary(t0, t1) if sampler is not None else None,
     }
     print(json.dumps(line), flush=True)
+
+
+def measure_configs(fa, dev, stream, peaks, iters=50):
+    """TFLOP/s of the smaller prefill configurations (single head N128, B1 H8 N1024 causal, B4 H16
+    N2048 d128 with 1 % of query rows x8, without and with the causal mask).  These are launch-bound,
+    so each is timed as a CUDA graph of `iters` launches, each after a 512 MiB write that flushes L2,
+    minus a graph of the writes alone, with CUDA events around the replays (median of 5).  Measured
+    outside the benchmark's timed region; the line's `value` stays the N8192 prefill."""
+    import torch
+    from exact_attention_31_gb300.workloads import WORKLOADS, make_workload
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream(dev)
+
+    def graph_ms(body):
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            body()  # eager once: fills the library's per-device caches before capture
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(iters):
+                body()
+        ts = []
+        for _ in range(6):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ts = sorted(ts[1:])
+        return ts[len(ts) // 2]
+
+    flush_ms = graph_ms(lambda: flush.zero_())
+    out = []
+    for name in ("prefill_b1h1_n128_d64", "prefill_b1h8_n1024_d64", "prefill_b4h16_n2048_d128"):
+        w = WORKLOADS[name]
+        q, k, v, _ = make_workload(w, dev)
+        o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        for causal in w.causal:
+            flops = 4.0 * w.B * w.H * w.Nq * w.Nk * w.d / (2 if causal else 1)
+
+            def body():
+                flush.zero_()
+                fa.fattn_fwd(q, k, v, causal=causal, scale=w.scale, out=o, lse=lse)
+
+            ms = max(graph_ms(body) - flush_ms, 1e-6) / iters
+            tf = flops / (ms * 1e-3) / 1e12
+            out.append({"workload": name + (" causal" if causal else ""), "ms": round(ms, 5),
+                        "tflops": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4)})
+        del q, k, v, o, lse
+    out.append({"method": f"CUDA graph of {iters} launches, each after a 512 MiB L2-flush write, minus a graph "
+                          f"of the writes alone; median of 5 replays"})
+    return out
 
 
 def run_e2e(fa, dev, stream, args, q, k, v, dq, dk, dv, scale_p, scale_d):
@@ -712,6 +769,8 @@ def main(argv=None):
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--e2e-steps", type=int, default=5, help="steps of the host-buffer run (0 = skip)")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the smaller prefill configurations (configs_measured)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
