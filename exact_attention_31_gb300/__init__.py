@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
     L.fattn_decode_host_workspace_size.restype = sz
     L.fattn_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
     L.fattn_decode_host.restype = i
+    L.fattn_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
+    L.fattn_fwd_fp8_workspace_size.restype = sz
+    L.fattn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, f, f, vp, sz, vp]
+    L.fattn_fwd_fp8.restype = i
     L.fattn_last_error.argtypes = [vp]
     L.fattn_last_error.restype = i
     L.fattn_status_string.argtypes = [i]
@@ -407,6 +411,49 @@ def fattn_decode_host(q, k_cache, v_cache, scale: float | None = None, out=None,
                                  workspace.numel() * workspace.element_size(), _stream_handle(stream, device))
     if st != FATTN_OK:
         raise FattnError(st, "fattn_decode_host")
+    return out, lse
+
+
+def fattn_fwd_fp8_workspace_size(B, H, Nk, d) -> int:
+    return lib().fattn_fwd_fp8_workspace_size(int(B), int(H), int(Nk), int(d))
+
+
+def fattn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, causal: bool = False,
+                  scale: float | None = None, window=None, out=None, lse=None, workspace=None, stream=None,
+                  want_lse: bool = True):
+    """Attention of q*q_descale, k*k_descale, v*v_descale (fattn_fwd_fp8): q, k, v are
+    torch.float8_e4m3fn [B,H,N,128] CUDA tensors; out bf16, lse fp32.  ``workspace`` (a CUDA uint8
+    tensor of fattn_fwd_fp8_workspace_size(...) bytes) receives V transposed; allocated here if
+    omitted.  Returns (out, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.float8_e4m3fn)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,H,Nq,d], k/v [B,H,Nk,d]")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q and k/v disagree on B, H or d")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(fattn_fwd_fp8_workspace_size(B, H, Nk, d), 256), dtype=torch.uint8,
+                                device=q.device)
+    _check(workspace, "workspace")
+    wl, wr = _band(causal, window)
+    st = lib().fattn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, wl, wr, float(scale),
+                             float(q_descale), float(k_descale), float(v_descale), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_fwd_fp8")
     return out, lse
 
 

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 
-SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu", "host_staging.cu"]
+SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "prefill_fp8_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu",
+           "host_staging.cu"]
 HEADERS = ["fattn_internal.h", "sm103a_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -117,6 +117,21 @@ bool make_map_f32(CUtensorMap* map, void* base, int BH, int rows, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D byte tensor [BH][rows][cols] (e4m3 operands), 128 x 128 boxes, 128-byte swizzle; out-of-range
+// elements read as zero.  cols and the row pitch are multiples of 16 bytes.
+bool make_map_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols) {
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows) * cols};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool positive_sizes(long long a, long long b, long long c, long long d) {
   return a >= 1 && b >= 1 && c >= 1 && d >= 1;
 }
@@ -315,6 +330,44 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
                                           align_up(parts * d * sizeof(float), 256));
   DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, 0};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+size_t fattn_fwd_fp8_workspace_size(int B, int H, int Nk, int d) {
+  if (!positive_sizes(B, H, Nk, 1) || d != 128) return 0;
+  return align_up(static_cast<size_t>(B) * H * d * fp8_padded_keys(Nk), 256);
+}
+
+fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                           int Nk, int d, int window_left, int window_right, float scale, float q_descale,
+                           float k_descale, float v_descale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !workspace) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nq, Nk) || window_left < -1 || window_right < -1) return FATTN_ERR_INVALID_ARG;
+  for (float x : {scale, q_descale, k_descale, v_descale})
+    if (!(x > 0.f) || !isfinite(x)) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL / 64 || Nk > 0x7fffffff - 128) return FATTN_ERR_INVALID_ARG;
+  if (d != 128) return FATTN_ERR_UNSUPPORTED;
+  const size_t need = fattn_fwd_fp8_workspace_size(B, H, Nk, d);
+  if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+  const int BH = B * H;
+  const int Nk_pad = fp8_padded_keys(Nk);
+  CUtensorMap tq, tk, tvt;
+  if (!make_map_u8(&tq, q, BH, Nq, d) || !make_map_u8(&tk, k, BH, Nk, d) || !make_map_u8(&tvt, workspace, BH, d, Nk_pad))
+    return FATTN_ERR_CUDA;
+  unsigned int* status = nullptr;
+  if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_vt_transpose(v, workspace, BH, Nk, s) != cudaSuccess) return FATTN_ERR_CUDA;
+  Fp8Problem p{q, k, workspace, o, lse, B, H, Nq, Nk, window_left, window_right, scale, q_descale, k_descale,
+               v_descale};
+  if (launch_prefill_fp8(p, tq, tk, tvt, status, wait_timeout_ns(), s) != cudaSuccess) return FATTN_ERR_CUDA;
   return FATTN_OK;
 }
 

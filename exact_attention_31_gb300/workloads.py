@@ -122,3 +122,20 @@ def make_dout(B: int, H: int, Nq: int, d: int, seed: int, device="cpu"):
     gen.manual_seed(int(seed) + DOUT_SEED_OFFSET)
     chunk = 1 if B * H * Nq * d > (1 << 28) else None
     return _randn_bf16((B, H, Nq, d), gen, device, chunk)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 quantisation of a float tensor: scale so that the largest magnitude maps to
+    448 (e4m3's largest finite value), round to nearest.  Returns (x_e4m3, descale) with
+    x ~ x_e4m3 * descale."""
+    amax = float(x.abs().max())
+    descale = amax / 448.0 if amax > 0 else 1.0
+    return (x.float() / descale).to(torch.float8_e4m3fn), descale
+
+
+def make_qkv_fp8(B: int, H: int, Nq: int, Nk: int, d: int, seed: int, device="cpu", boost_frac: float = 0.0):
+    """The bf16 inputs of make_qkv, each quantised to e4m3 with one descale factor per tensor.
+    Returns ((q8, k8, v8), (q_descale, k_descale, v_descale), boosted rows as in make_qkv)."""
+    q, k, v, boosted = make_qkv(B, H, Nq, Nk, d, seed, device, boost_frac)
+    out = [quantize_e4m3(t) for t in (q, k, v)]
+    return tuple(o[0] for o in out), tuple(o[1] for o in out), boosted

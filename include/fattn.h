@@ -206,6 +206,36 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
                                  void* stream);
 
 /*
+ * fattn_fwd_fp8 -- the attention forward on FP8 operands ("Flash Attention: The Hidden Gem", section
+ * FA1, FA2, FA3: FP8 support doubles the tensor-core rate at some cost in precision).  The pages
+ * state no accuracy contract for it; this one is stated from the arithmetic.
+ *
+ *   q        e4m3 [B, H, Nq, d]   (OCP FP8 E4M3: 1 sign, 4 exponent, 3 mantissa bits, bias 7)
+ *   k, v     e4m3 [B, H, Nk, d]
+ *   o        bf16 [B, H, Nq, d]; lse fp32 [B, H, Nq] or NULL, as for fattn_fwd_masked
+ *   q_descale, k_descale, v_descale   finite, > 0: the call computes the attention of the dequantised
+ *            tensors q * q_descale, k * k_descale, v * v_descale, with the band of fattn_fwd_masked
+ *            and the given scale
+ *   d        128 only (FATTN_ERR_UNSUPPORTED otherwise)
+ *   workspace  device memory of at least fattn_fwd_fp8_workspace_size(B, H, Nk, d) bytes, 256-byte
+ *            aligned, owned by the caller: it receives V transposed ([B*H][d][Nk rounded up to 16]),
+ *            because 8-bit operands are read by the tensor core with the reduced dimension contiguous.
+ *
+ * Both products are e4m3 x e4m3 with fp32 accumulation, so S is exact up to fp32 summation.  The
+ * probabilities enter P V rounded to e4m3 (relative error at most 2^-4 for weights above 2^-6 of the
+ * stored scale, an absolute error below 2^-10 of it under that); L and the normalisation use the
+ * fp32 weights.  Per output element, with p the exact probabilities of the dequantised problem:
+ *     |o - o_exact| <= 2^-4 * sum_j p_j |v_j| + 2^-9 |o_exact| + (2^-15 * n_j + 2^-16) * max_j |v_j|,
+ * n_j the row's visible keys (the last term covers weights stored below e4m3's normal range and the
+ * fp32 arithmetic); |lse - lse_exact| <= 2^-20 |lse| + 1e-5.  Calls sharing a workspace must not
+ * overlap.
+ */
+size_t fattn_fwd_fp8_workspace_size(int B, int H, int Nk, int d);
+fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                           int Nk, int d, int window_left, int window_right, float scale, float q_descale,
+                           float k_descale, float v_descale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fattn_fwd_host / fattn_decode_host -- the same computations with the inputs and outputs in HOST
  * memory.  The pages put the cost of attention in moving data between memory levels ("Flash
  * Attention: The Hidden Gem", Background; "FlashAttention: attention was never compute-bound",
