@@ -43,6 +43,7 @@ FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "prefill_sm103a.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "decode_sm103a.cu")
+PREFILL_FP8_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "prefill_fp8_sm103a.cu")
 BACKWARD_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "backward_sm103a.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
@@ -113,7 +114,7 @@ def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, or None when the kernel source has
     changed since the counters were taken.  Lines: `<kernel> <source-sha16> <bytes_per_launch>`."""
     src = {"prefill": PREFILL_KERNEL_SRC, "decode": DECODE_KERNEL_SRC, "backward64": BACKWARD_KERNEL_SRC,
-           "backward128": BACKWARD_KERNEL_SRC}[kernel]
+           "backward128": BACKWARD_KERNEL_SRC, "fp8": PREFILL_FP8_KERNEL_SRC}[kernel]
     try:
         digest = source_digest(src)
         with open(TRAFFIC_FILE) as f:
@@ -594,6 +595,96 @@ def run_backward(args):
     print(json.dumps(line), flush=True)
 
 
+def run_fp8(args):
+    """Time fattn_fwd_fp8 (V transpose + fused kernel) on B1 H32 N8192 d128 causal with e4m3 inputs.
+    A line of its own, outside the benchmark step: the step is the bf16 forward hot path."""
+    import torch
+    world, rank, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_31_gb300 as fa
+    from exact_attention_31_gb300.workloads import make_qkv_fp8
+    fa.lib()
+    B, H, N, d = 1, args.prefill_heads or 32, 8192, 128
+    stream = torch.cuda.current_stream(dev)
+    scale = 1 / math.sqrt(d)
+    (q, k, v), (qs, ks, vs), _ = make_qkv_fp8(B, H, N, N, d, 0xFA77E000 + 6, dev)
+    window = (args.window, 0) if args.window >= 0 else (-1, 0)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fattn_fwd_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        flush.zero_()
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fattn_fwd_fp8(q, k, v, qs, ks, vs, window=window, scale=scale, out=o, lse=lse, workspace=ws, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for_smi(dev)).start() if args.clocks else None
+    if sampler is not None:
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    if sampler is not None:
+        time.sleep(0.15)
+        sampler.stop()
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    avg = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, dist, dev)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    pairs = visible_pairs(N, args.window) if args.window >= 0 else N * N / 2  # the causal convention
+    fl = 4.0 * B * H * d * pairs
+    tf = fl / (avg * 1e-3) / 1e12
+    fp8_peak = 2 * peaks["bf16_tflops"]
+    line = {
+        "metric": "attn fwd TFLOP/s, FP8 e4m3 operands (fattn_fwd_fp8: V transpose + fused kernel)",
+        "value": round(world * tf, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic: seeded iid N(0,1) rounded to bf16, then per-tensor e4m3 quantisation",
+        "config": {"workload": f"prefill_fp8_b{B}h{H}_n{N}_d{d} causal" +
+                               (f" sliding window {args.window + 1}" if args.window >= 0 else ""),
+                   "fp8": {"B": B, "H": H, "Nq": N, "Nk": N, "d": d, "band": list(window), "scale": scale,
+                           "descales": [qs, ks, vs], "flops_per_call": fl},
+                   "l2": "a 512 MiB buffer is written before every call (outside the per-call events)",
+                   "parallelism": f"replicas x{world}"},
+        "fp8_ms": round(avg, 4),
+        "roofline": {"kernel": "fattn_fwd_fp8 (fwd_fp8_vt_kernel + prefill_fp8_kernel)", "bound": "tensor",
+                     "achieved": round(tf, 2), "peak": fp8_peak, "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
+                     "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM) x 2, the nominal fp8:bf16 ratio",
+                     "traffic": recorded_traffic("fp8") if (B, H, N) == (1, 32, 8192) and args.window < 0 else None,
+                     "traffic_kernel": "prefill_fp8_kernel alone (ncu)",
+                     "algorithmic_bytes": B * H * N * d * 3 + B * H * N * d * 2 + B * H * N * 4},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(t0, t1) if sampler is not None else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def measure_configs(fa, dev, stream, peaks, iters=50):
     """TFLOP/s of the smaller prefill configurations (single head N128, B1 H8 N1024 causal, B4 H16
     N2048 d128 with 1 % of query rows x8, without and with the causal mask).  These are launch-bound,
@@ -755,7 +846,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["both", "prefill", "decode", "backward"], default="both",
+    ap.add_argument("--workload", choices=["both", "prefill", "decode", "backward", "fp8"], default="both",
                     help="both = the benchmark step; prefill/decode time one half (profiling); backward "
                          "times fattn_bwd on the prefill shape (a line of its own)")
     ap.add_argument("--bwd-d", type=int, default=0, help="override d of the backward workload (64 or 128)")
@@ -778,6 +869,8 @@ def main(argv=None):
         run_reference(args)
     elif args.workload == "backward":
         run_backward(args)
+    elif args.workload == "fp8":
+        run_fp8(args)
     else:
         run_ours(args)
 
