@@ -140,8 +140,8 @@ size_t fattn_decode_workspace_size(int B, int H, int Nk, int d, int num_splits);
 
 /*
  * fattn_decode -- one query token per (b, h) against a KV cache (Nq = 1; "Understanding
- * FlashAttention", Attention: "when decoding one token, N = 1").  No mask: every cached key is
- * visible.
+ * FlashAttention", Attention: decoding a single token is the case of one query row).  No mask:
+ * every cached key is visible.
  *
  *   q        bf16 [B, H, 1, d]
  *   k_cache  bf16 [B, H, Nk, d]
