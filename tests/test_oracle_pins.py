@@ -370,7 +370,8 @@ def _tiled_forward(Q, K, V, scale, Br, Bc, causal=False, window=None):
 
 @pytest.mark.parametrize("n", [128, 256, 1024])
 def test_tiled_equals_oracle_to_fp64_noise(n):
-    # the tiling demo of [IO]: tiled and standard attention agree to fp64 rounding (~1e-16)
+    # "FlashAttention: attention was never compute-bound", tiling demo: tiled and standard attention
+    # agree to fp64 rounding (~1e-16)
     rng = np.random.default_rng(22 + n)
     d = 64
     Q, K, V = (rng.standard_normal((n, d)) for _ in range(3))
