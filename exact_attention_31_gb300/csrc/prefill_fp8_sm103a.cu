@@ -581,7 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // V [BH][Nk][128] -> V^T [BH][128][Nk_pad] (e4m3 bytes), keys Nk .. Nk_pad - 1 written as zero.
-// One block per (128-key tile, head): 128 x 128 bytes through shared memory, 16-byte loads and stores.
+// One block per (128-key tile, head): the tile is read with 16-byte loads into shared memory; thread
+// (key block kb of 16 keys, word w = 4 d values) reads its 16 words (conflict-free: a warp reads 32
+// words of one row), transposes four 4 x 4 byte blocks with byte permutes, and writes 16 keys of
+// each of its 4 d rows as one 16-byte store.
 __global__ void __launch_bounds__(256) fwd_fp8_vt_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
                                                          int Nk, int Nk_pad) {
   __shared__ uint32_t tile[128][33];  // [key][d / 4], padded
@@ -598,24 +601,25 @@ __global__ void __launch_bounds__(256) fwd_fp8_vt_kernel(const uint8_t* __restri
     tile[key][4 * c + 3] = w.w;
   }
   __syncthreads();
-  uint8_t* dst = vt + static_cast<size_t>(bh) * kD * Nk_pad;
-  for (int i = threadIdx.x; i < 128 * 8; i += 256) {
-    const int t = i >> 3, c = i & 7;  // d row t, keys key0 + 16c .. + 15
-    if (key0 + 16 * c >= Nk_pad) continue;
-    uint32_t out[4];
+  const int w = threadIdx.x & 31, kb = threadIdx.x >> 5;  // d values 4w .. 4w + 3, keys 16kb .. 16kb + 15
+  if (key0 + 16 * kb >= Nk_pad) return;
+  uint32_t out[4][4];  // [d row r][word: 4 keys]
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t x = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t word = tile[16 * c + 4 * w + b][t >> 2];
-        x |= ((word >> (8 * (t & 3))) & 0xFFu) << (8 * b);
-      }
-      out[w] = x;
-    }
-    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(t) * Nk_pad + key0 + 16 * c) =
-        make_uint4(out[0], out[1], out[2], out[3]);
+  for (int b4 = 0; b4 < 4; ++b4) {
+    const uint32_t a0 = tile[16 * kb + 4 * b4][w], a1 = tile[16 * kb + 4 * b4 + 1][w];
+    const uint32_t a2 = tile[16 * kb + 4 * b4 + 2][w], a3 = tile[16 * kb + 4 * b4 + 3][w];
+    const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+    const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+    out[0][b4] = __byte_perm(t0, t2, 0x5410);
+    out[1][b4] = __byte_perm(t0, t2, 0x7632);
+    out[2][b4] = __byte_perm(t1, t3, 0x5410);
+    out[3][b4] = __byte_perm(t1, t3, 0x7632);
   }
+  uint8_t* dst = vt + static_cast<size_t>(bh) * kD * Nk_pad + key0 + 16 * kb;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(4 * w + r) * Nk_pad) =
+        make_uint4(out[r][0], out[r][1], out[r][2], out[r][3]);
 }
 
 }  // namespace
