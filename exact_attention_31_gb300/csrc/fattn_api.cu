@@ -366,7 +366,7 @@ fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_vt_transpose(v, workspace, BH, Nk, s) != cudaSuccess) return FATTN_ERR_CUDA;
   Fp8Problem p{q, k, workspace, o, lse, B, H, Nq, Nk, window_left, window_right, scale, q_descale, k_descale,
-               v_descale};
+               v_descale, test_drop_kv_block()};
   if (launch_prefill_fp8(p, tq, tk, tvt, status, wait_timeout_ns(), s) != cudaSuccess) return FATTN_ERR_CUDA;
   return FATTN_OK;
 }

@@ -95,6 +95,7 @@ struct Fp8Problem {
   int B, H, Nq, Nk;
   int window_left, window_right;
   float scale, q_descale, k_descale, v_descale;
+  int drop_kv_block;  // failure-detection testing only: key tile never loaded (-1 = off)
 };
 
 int fp8_padded_keys(int Nk);

@@ -75,6 +75,7 @@ struct F8Args {
   float v_descale;
   unsigned int* status;
   unsigned long long timeout_ns;
+  int drop_kv_block;  // failure-detection testing only; -1 = off
 };
 
 // Key tiles [jb, je) that query tile [r0, r0 + 128) visits (empty past Nq or outside the band).
@@ -356,6 +357,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
   tma_prefetch_desc(tk);
   tma_prefetch_desc(tvt);
   int ring = 0, issued = 0;
+  int dropped = -1;  // ring index of the load skipped for failure-detection testing
   int qloads[2] = {0, 0};
   bool ok = true;
   Unit u;
@@ -384,6 +386,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
           ok = false;
           break;
         }
+        if (w == 0 && j == a.drop_kv_block) {  // testing only: this tile never arrives
+          dropped = idx;
+          issued = idx + 1;
+          continue;
+        }
         const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
         mbar_arrive_expect_tx(bar, kTileBytes);
         const uint32_t dst = sbase + C::kKVOff + slot * kTileBytes;
@@ -398,7 +405,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
     const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
     volatile uint32_t never = 0;
     for (int idx = max(0, issued - kSlots); idx < issued; ++idx)
-      mbar_wait_bounded(sbar + 8 * (C::kKVFull + idx % kSlots), (idx / kSlots) & 1, &never, until);
+      if (idx != dropped)
+        mbar_wait_bounded(sbar + 8 * (C::kKVFull + idx % kSlots), (idx / kSlots) & 1, &never, until);
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
       if (qloads[t] > 0) mbar_wait_bounded(sbar + 8 * (C::kQFull + t), (qloads[t] - 1) & 1, &never, until);
@@ -667,6 +675,7 @@ cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const
   a.v_descale = p.v_descale;
   a.status = status;
   a.timeout_ns = timeout_ns;
+  a.drop_kv_block = p.drop_kv_block;
   const unsigned int grid = static_cast<unsigned int>(min(a.total_units, sm_count[dev]));
   prefill_fp8_kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tvt, a);
   return cudaGetLastError();

@@ -1,6 +1,6 @@
 """Failure detection without a GPU fault.
 
-Every wait in the prefill and backward kernels is bounded.  A wait that gives up sets the library's device
+Every wait in the prefill (bf16 and FP8) and backward kernels is bounded.  A wait that gives up sets the library's device
 status word, and the kernel then winds down: in-flight copies land, MMAs drain, TMEM is freed.
 The host reads the word with fattn_last_error.  The test makes one wait run out: a test-only switch
 (FATTN_TEST_DROP_KV_BLOCK) stops the producer from loading one key tile, so nothing ever completes
@@ -90,3 +90,37 @@ def test_bounded_wait_reports_timeout_and_context_survives():
                        timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "FAILURE-DETECTION-OK" in r.stdout
+
+
+CHILD_FP8 = r"""
+import math, sys
+sys.path.insert(0, sys.argv[1])
+sys.path.insert(0, sys.argv[1] + "/tests")
+import torch
+import exact_attention_31_gb300 as fa
+from exact_attention_31_gb300.workloads import make_qkv, make_qkv_fp8
+from parity_utils import compare, oracle_full
+
+(q8, k8, v8), (qs, ks, vs), _ = make_qkv_fp8(1, 2, 512, 512, 128, seed=11, device="cuda")
+fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)   # key tile 1 is never loaded
+torch.cuda.synchronize()
+assert fa.fattn_last_error() == fa.FATTN_ERR_TIMEOUT
+assert fa.fattn_last_error() == fa.FATTN_OK
+
+dq, dk, dv, _ = make_qkv(1, 2, 1, 300, 128, seed=12, device="cuda")
+od, ld = fa.fattn_decode(dq, dk, dv)
+torch.cuda.synchronize()
+o_ref, l_ref = oracle_full(dq, dk, dv, False, 1 / math.sqrt(128))
+compare(od, ld, o_ref, l_ref, what="decode after a reported FP8 timeout")
+assert fa.fattn_last_error() == fa.FATTN_OK
+print("FAILURE-DETECTION-FP8-OK")
+"""
+
+
+@pytest.mark.gpu
+def test_fp8_bounded_wait_reports_timeout_and_context_survives():
+    env = dict(os.environ, FATTN_WAIT_TIMEOUT_MS="200", FATTN_TEST_DROP_KV_BLOCK="1")
+    r = subprocess.run([sys.executable, "-c", CHILD_FP8, ROOT], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "FAILURE-DETECTION-FP8-OK" in r.stdout

@@ -124,3 +124,28 @@ def test_fp8_rejects_other_head_dims(fa):
     with pytest.raises(fa.FattnError) as e:
         fa.fattn_fwd_fp8(q, q, q, 1.0, 1.0, 1.0, workspace=torch.empty(4096, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 2
+
+
+def _random_cases(n=12, seed=0xF8):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        Nq, Nk = int(rng.integers(1, 600)), int(rng.integers(1, 600))
+        kind = int(rng.integers(0, 4))
+        band = [(-1, -1), (-1, 0), (int(rng.integers(0, 300)), 0),
+                (int(rng.integers(0, 200)), int(rng.integers(0, 200)))][kind]
+        out.append((B, H, Nq, Nk, band))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "b{}h{}q{}k{}w{}_{}".format(*c[:4], *c[4]))
+def test_fp8_random_shapes_within_stated_bound(fa, case):
+    from exact_attention_31_gb300.workloads import make_qkv_fp8
+    B, H, Nq, Nk, band = case
+    (q8, k8, v8), (qs, ks, vs), _ = make_qkv_fp8(B, H, Nq, Nk, 128, 9300 + 3 * Nq + Nk, device="cuda")
+    scale = 0.9 / math.sqrt(128)
+    o, lse = fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, window=band, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    check_bound(o, lse, _deq(q8, qs), _deq(k8, ks), _deq(v8, vs), band, scale, what=str(case))
