@@ -26,6 +26,7 @@ __all__ = [
     "fattn_decode_static",
     "fattn_decode_num_splits",
     "fattn_decode_workspace_size",
+    "fattn_fwd_recomputed_rows",
     "fattn_last_error",
     "fattn_status_string",
     "lib",
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
     L.fattn_fwd_fp8.restype = i
     L.fattn_last_error.argtypes = [vp]
     L.fattn_last_error.restype = i
+    L.fattn_fwd_recomputed_rows.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+    L.fattn_fwd_recomputed_rows.restype = i
     L.fattn_status_string.argtypes = [i]
     L.fattn_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -455,6 +458,16 @@ def fattn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float,
     if st != FATTN_OK:
         raise FattnError(st, "fattn_fwd_fp8")
     return out, lse
+
+
+def fattn_fwd_recomputed_rows() -> int:
+    """Rows the forward recomputed on its exact per-row path on the current device so far (waits
+    for the device)."""
+    out = ctypes.c_ulonglong(0)
+    st = lib().fattn_fwd_recomputed_rows(ctypes.byref(out))
+    if st != 0:
+        raise FattnError(st, "fattn_fwd_recomputed_rows")
+    return int(out.value)
 
 
 def fattn_last_error(stream=None) -> int:

@@ -18,6 +18,8 @@ namespace {
 
 // Status word the kernels raise bits in (bounded waits that gave up).  One copy per device.
 __device__ unsigned int g_device_status;
+// Rows of fattn_fwd that the prefill kernel recomputed on its exact per-row path (cumulative).
+__device__ unsigned long long g_recomputed_rows;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -68,6 +70,26 @@ cudaError_t device_status_ptr(unsigned int** out) {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned int*>(p);
   *out = static_cast<unsigned int*>(p);
+  return cudaSuccess;
+}
+
+// Device address of g_recomputed_rows for the current device, looked up once per device.
+cudaError_t recomputed_rows_ptr(unsigned long long** out) {
+  static std::mutex mu;
+  static unsigned long long* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && cache[dev] != nullptr) {
+    *out = cache[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_recomputed_rows);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned long long*>(p);
+  *out = static_cast<unsigned long long*>(p);
   return cudaSuccess;
 }
 
@@ -178,8 +200,10 @@ fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, floa
   if (!make_map(&tq, q, BH, Nq, d) || !make_map(&tk, k, BH, Nk, d) || !make_map(&tv, v, BH, Nk, d))
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
-  if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
-  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, wl, wr, scale, test_drop_kv_block()};
+  unsigned long long* recomputed = nullptr;
+  if (device_status_ptr(&status) != cudaSuccess || recomputed_rows_ptr(&recomputed) != cudaSuccess)
+    return FATTN_ERR_CUDA;
+  FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, wl, wr, scale, test_drop_kv_block(), recomputed};
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
@@ -438,6 +462,15 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
   float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(parts * d * sizeof(float), 256));
   DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, 0};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+fattn_status fattn_fwd_recomputed_rows(unsigned long long* out) {
+  if (out == nullptr) return FATTN_ERR_INVALID_ARG;
+  unsigned long long* p = nullptr;
+  if (recomputed_rows_ptr(&p) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaMemcpy(out, p, sizeof(*out), cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
   return FATTN_OK;
 }
 

@@ -27,6 +27,8 @@ struct FwdProblem {
   // Failure-detection testing only (never set in normal use): the key tile of this block index is
   // not loaded, so the waits for it must give up and report a timeout.  -1 = off.
   int drop_kv_block;
+  // Device counter of rows recomputed on the exact per-row path (incremented by the kernel).
+  unsigned long long* recomputed;
 };
 
 struct DecodeProblem {

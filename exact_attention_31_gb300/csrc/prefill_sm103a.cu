@@ -1,10 +1,12 @@
 // prefill_sm103a.cu -- fused exact attention forward for sm_103a (tcgen05 + TMEM + TMA).
 //
 // What it computes is the FlashAttention-2 forward loop nest ("Flash Attention: The Hidden Gem",
-// The Algorithm, steps 3-7): for each query tile, carry a running max m, a running sum l and an
-// unnormalised output O per row; for each key/value tile compute S = Q K^T, raise m, rescale l and
-// O by exp(m_old - m_new) (The Correction Factor), add P = exp(S - m) and P V; after the last tile
-// write O / l and L = m + log(l).  S and P live only in tensor memory.
+// The Algorithm, steps 3-7): for each query tile, carry an exponent reference m, a running sum l and
+// an unnormalised output O per row; for each key/value tile compute S = Q K^T, add P = exp(S - m)
+// to l and P V to O; after the last tile write O / l and L = m + log(l).  S and P live only in
+// tensor memory.  The pages raise m to the running max at every tile and rescale l and O by
+// exp(m_old - m_new) (The Correction Factor); here m is set once per row and the rows whose weights
+// would leave the safe range are recomputed (see below), which gives the same result.
 //
 // The grid is persistent: at most one CTA per SM, each working through units (two adjacent 128-row
 // query tiles of one (b, h)) in rounds, heaviest causal units first.  Every barrier counts its
@@ -30,15 +32,21 @@
 // CTA let the tensor core work on one tile while the other tile's softmax runs.
 //
 // Scores are handled in log2 units: with c = scale * log2(e), exp(scale * s - scale * m) is
-// exp2(s * c - m * c), one FFMA and one ex2 per element.  The running max used as the exponent
-// reference is only raised when the tile max exceeds it by more than kRescaleLog2 (the rescale is
-// exact for any reference as long as l, O and L use the same one: exp(a-c) = exp(a-b) exp(b-c),
-// "FlashAttention: attention was never compute-bound", On the maths anxiety), which keeps most
-// tiles from touching O in TMEM at all.  One row sum l of the fp32 weights gives both O / l and
-// L = m + log(l); P V sees the weights rounded to bf16, so O carries a relative bias of at most
-// 2^-9 (one rounding of the dominant weight) on rows with one dominant key.  The per-row arithmetic uses packed
-// fp32x2 FMA/add and three-input max with several independent accumulators, so one thread's row
-// is not a single long dependency chain.
+// exp2(s * c - m * c), one FFMA and one ex2 per element.  The exponent reference m of a row is the
+// max of its first key tile that holds a visible key, and it stays there: the result is the same
+// for any reference as long as l, O and L use the same one (exp(a-c) = exp(a-b) exp(b-c),
+// "FlashAttention: attention was never compute-bound", On the maths anxiety), and fp32 and bf16
+// keep their relative precision over the whole normal range, so a later key tile whose scores rise
+// above m only makes its weights larger than 1.  That saves the row max and the O correction of
+// every later step.  What it gives up is a bound on the weights, so each row is checked when its
+// unit ends: with the reference in place its weight sum l is at least 1 (the first max has weight
+// 1), and the row is accepted when l <= 2^64 and every output is finite.  A row that fails (its
+// scores rose by more than about 64 / c over those of its first tile) is recomputed by its own
+// thread in fp32 with an exact max and plain loads, and counted in a device counter.  One row sum
+// l of the fp32 weights gives both O / l and L = m + log(l); P V sees the weights rounded to bf16,
+// so O carries a relative bias of at most 2^-9 (one rounding of the dominant weight) on rows with
+// one dominant key.  The per-row arithmetic uses packed fp32x2 FMA/add and three-input max with
+// several independent accumulators, so one thread's row is not a single long dependency chain.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -55,7 +63,7 @@ constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;   // tile 0 (d = 64) or both tiles (d = 128); TMEM owner
 constexpr int kMmaWarp1 = 10; // tile 1 (d = 64)
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kWeightSumMax = 0x1p64f;  // a row whose weight sum exceeds this is recomputed
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtomBytes = kBlockM * 128;  // one 128-row x 128-byte swizzled chunk
 
@@ -72,7 +80,7 @@ struct Cfg {
   static constexpr int kQFull = 0;              // [2] Q_t landed
   static constexpr int kSFull = 2;              // [2] S_t computed
   static constexpr int kSFree = 4;              // [2] S_t read into registers (separate-P only)
-  static constexpr int kPFull = 6;              // [2] P_t written, O_t corrected
+  static constexpr int kPFull = 6;              // [2] P_t written
   static constexpr int kPVDone = 8;             // [2] O_t += P_t V done (separate-P only)
   static constexpr int kOFull = 10;             // [2] last P V of tile t done
   static constexpr int kQFree = 12;             // [2] the unit's last S_t has read Q_t
@@ -92,6 +100,9 @@ struct Cfg {
 };
 
 struct Args {
+  const __nv_bfloat16* q;  // [BH, Nq, D], for rows that are recomputed
+  const __nv_bfloat16* k;  // [BH, Nk, D]
+  const __nv_bfloat16* v;  // [BH, Nk, D]
   __nv_bfloat16* o;
   float* lse;
   int BH, Nq, Nk;
@@ -100,6 +111,7 @@ struct Args {
   int total_units;     // BH * units_per_head
   float c_log2;        // scale * log2(e)
   unsigned int* status;
+  unsigned long long* recomputed;  // rows recomputed by recompute_row (diagnostic counter)
   unsigned long long timeout_ns;
   int drop_kv_block;  // failure-detection testing only; -1 = off
 };
@@ -221,6 +233,57 @@ __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) 
 }
 
 // ------------------------------------------------------------------------------------------------
+// One row recomputed by its own thread: O = softmax(scale * q K^T) V over the visible keys
+// [kb, ke] and L, in fp32 from the bf16 inputs with an exact max.  Two passes give the max and the
+// weight sum, then one pass per 32 output columns accumulates P V (each pass recomputes the
+// scores, so only 32 accumulators are live).  Plain loads, O(Nk d) work per row: it serves only
+// the rows the fast path rejected.
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ __noinline__ void recompute_row(const Args& a, int bh, int row, int kb, int ke) {
+  const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(a.q + (static_cast<size_t>(bh) * a.Nq + row) * D);
+  const __nv_bfloat16* kh = a.k + static_cast<size_t>(bh) * a.Nk * D;
+  const __nv_bfloat16* vh = a.v + static_cast<size_t>(bh) * a.Nk * D;
+  const float c = a.c_log2;
+  auto score = [&](int j) {  // q . k_j * c
+    const __nv_bfloat162* kr = reinterpret_cast<const __nv_bfloat162*>(kh + static_cast<size_t>(j) * D);
+    float s0 = 0.f, s1 = 0.f;
+    for (int e = 0; e < D / 2; ++e) {
+      const float2 x = __bfloat1622float2(q[e]), y = __bfloat1622float2(kr[e]);
+      s0 = fmaf(x.x, y.x, s0);
+      s1 = fmaf(x.y, y.y, s1);
+    }
+    return (s0 + s1) * c;
+  };
+  float m = -INFINITY;
+  for (int j = kb; j <= ke; ++j) m = fmaxf(m, score(j));
+  float l = 0.f;
+  for (int j = kb; j <= ke; ++j) l += exp2f(score(j) - m);
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + row) * D;
+  for (int d0 = 0; d0 < D; d0 += 32) {
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+    for (int j = kb; j <= ke; ++j) {
+      const float p = exp2f(score(j) - m);
+      const __nv_bfloat162* vr = reinterpret_cast<const __nv_bfloat162*>(vh + static_cast<size_t>(j) * D + d0);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float2 y = __bfloat1622float2(vr[e]);
+        acc[2 * e] = fmaf(p, y.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(p, y.y, acc[2 * e + 1]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) orow[d0 + e] = __float2bfloat16_rn(acc[e] * inv_l);
+  }
+  if (a.lse != nullptr)
+    a.lse[static_cast<size_t>(bh) * a.Nq + row] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+  atomicAdd(a.recomputed, 1ull);
+}
+
+// ------------------------------------------------------------------------------------------------
 // Softmax group: one thread per query row.
 // ------------------------------------------------------------------------------------------------
 // g counts tile t's steps over all units of this CTA (the phase of S_full, P_full, PV_done);
@@ -243,7 +306,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   const uint32_t tP = tmem + lane_field + C::col_p(t);
   const float c = a.c_log2;
 
-  float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
+  float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score (set once per unit)
   float l = 0.f;            // sum of the fp32 weights: O = O / l, L = m + log(l)
   bool ok = true;
   for (int step = 0; step < n_tiles; ++step, ++g) {
@@ -273,26 +336,22 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
         for (int i = 0; i < 32; ++i)
           if (kv0 + 32 * h + i > hi || kv0 + 32 * h + i < lo) s[h][i] = __float_as_uint(-INFINITY);
     }
-    // row max: eight independent three-input chains
-    float mx8[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[0][2 * k]), __uint_as_float(s[0][2 * k + 1]));
-#pragma unroll
-    for (int e = 16; e < 128; e += 16) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mx8[k] = max3f(mx8[k], __uint_as_float(s[(e + 2 * k) >> 5][(e + 2 * k) & 31]),
-                       __uint_as_float(s[(e + 2 * k + 1) >> 5][(e + 2 * k + 1) & 31]));
-    }
-    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), fmaxf(max3f(mx8[3], mx8[4], mx8[5]),
-                                                                max3f(mx8[6], mx8[7], mx8[7])));
-    const float m_new = fmaxf(m_ref, mx * c);
-    const bool need = m_new > m_ref + kRescaleLog2;
-    float corr = 1.f;
-    if (need) {
-      corr = ex2_approx(m_ref - m_new);  // 0 on the first tile
-      m_ref = m_new;
-      l *= corr;
+    // The reference is the max of the row's first key tile that holds a visible key (eight
+    // independent three-input chains); later tiles leave it in place.
+    if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+      float mx8[8];
+  #pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[0][2 * k]), __uint_as_float(s[0][2 * k + 1]));
+  #pragma unroll
+      for (int e = 16; e < 128; e += 16) {
+  #pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mx8[k] = max3f(mx8[k], __uint_as_float(s[(e + 2 * k) >> 5][(e + 2 * k) & 31]),
+                         __uint_as_float(s[(e + 2 * k + 1) >> 5][(e + 2 * k + 1) & 31]));
+      }
+      const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), fmaxf(max3f(mx8[3], mx8[4], mx8[5]),
+                                                                  max3f(mx8[6], mx8[7], mx8[7])));
+      if (m_ref == -INFINITY) m_ref = mx * c;
     }
     const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
@@ -328,23 +387,6 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     }
     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
-    // Rescale O_t (last written by P_t(j-1) V_{j-1}, now complete) when the reference moved.
-    if (step > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-      for (int h = 0; h < D / 32; ++h) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tO + 32 * h, o);
-        wait_dep(o);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float y0, y1;
-          ffma2_bc(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), corr, 0.f);
-          o[i] = __float_as_uint(y0);
-          o[i + 1] = __float_as_uint(y1);
-        }
-        tmem_st_32x32b_x32(tO + 32 * h, o);
-      }
-    }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -368,6 +410,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   tc_fence_after();
   // A row that saw no key has l = 0 and m = -inf: o = 0 and L = -inf.
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  float fin = 0.f;  // sum of the outputs / 256: not finite iff one of them is not
 #pragma unroll
   for (int h = 0; h < D / 32; ++h) {
     uint32_t o[32];
@@ -375,8 +418,11 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     wait_dep(o);
     uint32_t pk[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    for (int i = 0; i < 16; ++i) {
+      const float y0 = __uint_as_float(o[2 * i]) * inv_l, y1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+      fin = fmaf(y0, 0x1p-8f, fmaf(y1, 0x1p-8f, fin));
+      pk[i] = pack_bf16x2(y0, y1);
+    }
     if (store) {
       uint4* dst = reinterpret_cast<uint4*>(orow + 32 * h);
 #pragma unroll
@@ -391,6 +437,13 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   if (store && a.lse != nullptr) {
     a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
+  // A row with a visible key has l >= 1 (the reference's own weight); it is accepted when l stayed
+  // within kWeightSumMax (no weight overflowed or approached the fp32 range) and its outputs are
+  // finite.  Otherwise its thread recomputes it.
+  const int k_lo = max(lo, 0);
+  const bool accepted = l >= 0.5f && l <= kWeightSumMax && fabsf(fin) <= 3.4028234663852886e38f;
+  if (store && k_lo <= hi && !accepted) recompute_row<D>(a, bh, q_row, k_lo, hi);
+  __syncwarp();
   return true;
 }
 
@@ -751,6 +804,9 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   Args a;
+  a.q = static_cast<const __nv_bfloat16*>(p.q);
+  a.k = static_cast<const __nv_bfloat16*>(p.k);
+  a.v = static_cast<const __nv_bfloat16*>(p.v);
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.lse = p.lse;
   a.BH = p.B * p.H;
@@ -763,6 +819,7 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.total_units = a.units_per_head * a.BH;
   a.c_log2 = p.scale * 1.4426950408889634f;
   a.status = status;
+  a.recomputed = p.recomputed;
   a.timeout_ns = timeout_ns;
   a.drop_kv_block = p.drop_kv_block;
   // Persistent: one CTA per SM (each holds all of an SM's tensor memory), looping over the units.
