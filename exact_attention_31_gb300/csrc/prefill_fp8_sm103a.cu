@@ -232,11 +232,22 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     for (int h = 0; h < 4; ++h) wait_dep(s[h]);
     const int kv0 = j * kBlockN;
     if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > hi || kv0 < lo)) {
+      // Keys past this row's visible range, as offsets into the tile: one compare with an
+      // immediate per key, and no lower-side compare when the band has no lower bound (causal).
+      const int vhi = hi - kv0, vlo = lo - kv0;
+      if (a.wl < 0) {
 #pragma unroll
-      for (int h = 0; h < 4; ++h)
+        for (int h = 0; h < 4; ++h)
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (kv0 + 32 * h + i > hi || kv0 + 32 * h + i < lo) s[h][i] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 32; ++i)
+            if (32 * h + i > vhi) s[h][i] = __float_as_uint(-INFINITY);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
+      }
     }
     float mx8[8];
 #pragma unroll
