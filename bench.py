@@ -465,8 +465,8 @@ def run_ours(args):
     if do_decode:
         dec_bw = decode_bytes(D["B"], D["H"], D["Nk"], D["d"]) / (dec_avg * 1e-3) / 1e9
         line["config"]["decode"] = {"B": D["B"], "H": D["H"], "Nq": 1, "Nk": D["Nk"], "d": D["d"],
-                                    "causal": False, "num_splits": fa.fattn_decode_num_splits(D["Nk"], 0),
-                                    "partial_states": "one (m, l, O) per 64-key block",
+                                    "causal": False, "num_splits": fa.fattn_decode_num_splits(D["B"], D["H"], D["Nk"], 0),
+                                    "partial_states": "one (m, l, O) per split of about 512 keys (8 blocks of 64)",
                                     "kv_bytes_per_launch": kv}
         line["decode"] = {"value": round(world * kv / (dec_avg * 1e-3) / 1e9, 1), "unit": "GB/s",
                           "ms": round(dec_avg, 4), "frac_of_hbm": round(dec_bw / peaks["hbm_gbs"], 4)}

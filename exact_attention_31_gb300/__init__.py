@@ -70,7 +70,7 @@ def lib() -> ctypes.CDLL:
     L.fattn_bwd.restype = i
     L.fattn_bwd_masked.argtypes = [vp] * 9 + [i, i, i, i, i, i, i, f, vp, sz, vp]
     L.fattn_bwd_masked.restype = i
-    L.fattn_decode_num_splits.argtypes = [i, i]
+    L.fattn_decode_num_splits.argtypes = [i, i, i, i]
     L.fattn_decode_num_splits.restype = i
     L.fattn_decode_workspace_size.argtypes = [i, i, i, i, i]
     L.fattn_decode_workspace_size.restype = sz
@@ -222,8 +222,8 @@ def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None
     return dq, dk, dv
 
 
-def fattn_decode_num_splits(Nk: int, num_splits: int = 0) -> int:
-    return lib().fattn_decode_num_splits(int(Nk), int(num_splits))
+def fattn_decode_num_splits(B: int, H: int, Nk: int, num_splits: int = 0) -> int:
+    return lib().fattn_decode_num_splits(int(B), int(H), int(Nk), int(num_splits))
 
 
 def fattn_decode_workspace_size(B: int, H: int, Nk: int, d: int, num_splits: int = 0) -> int:

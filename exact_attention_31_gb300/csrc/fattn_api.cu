@@ -8,6 +8,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "fattn.h"
@@ -288,17 +289,24 @@ fattn_status fattn_bwd_masked(const void* q, const void* k, const void* v, const
                   workspace_bytes, stream);
 }
 
-int fattn_decode_num_splits(int Nk, int num_splits) {
-  if (Nk < 1) return -1;
+int fattn_decode_num_splits(int B, int H, int Nk, int num_splits) {
+  if (B < 1 || H < 1 || Nk < 1) return -1;
   const int nblk = (Nk + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
-  if (num_splits == 0) return nblk;
+  if (num_splits == 0) {
+    // Splits of about 8 blocks, or more of them (up to one per block) while fewer than 8192
+    // (b, h, split) warps would be left to spread over the GPU.
+    const long long bh = static_cast<long long>(B) * H;
+    const long long by_length = (nblk + 7) / 8;
+    const long long by_width = (8192 + bh - 1) / bh;
+    return static_cast<int>(std::min<long long>(nblk, std::max(by_length, by_width)));
+  }
   if (num_splits < 0 || num_splits > nblk) return -1;
   return num_splits;
 }
 
 size_t fattn_decode_workspace_size(int B, int H, int Nk, int d, int num_splits) {
   if (!positive_sizes(B, H, Nk, d)) return 0;
-  const int S = fattn_decode_num_splits(Nk, num_splits);
+  const int S = fattn_decode_num_splits(B, H, Nk, num_splits);
   if (S < 1) return 0;
   const size_t parts = static_cast<size_t>(B) * H * S;
   return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256);
@@ -319,7 +327,7 @@ fattn_status fattn_decode_masked(const void* q, const void* k_cache, const void*
   if (!positive_sizes(B, H, Nk, 1)) return FATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
-  const int S = fattn_decode_num_splits(Nk - key_lo, num_splits);
+  const int S = fattn_decode_num_splits(B, H, Nk - key_lo, num_splits);
   if (S < 1) return FATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H * S > 0x7fffffffLL) return FATTN_ERR_INVALID_ARG;
   const size_t need = fattn_decode_workspace_size(B, H, Nk - key_lo, d, num_splits);
@@ -343,7 +351,7 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
   if (!positive_sizes(B, H, Nk, 1)) return FATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
-  const int S = fattn_decode_num_splits(Nk, num_splits);
+  const int S = fattn_decode_num_splits(B, H, Nk, num_splits);
   if (S < 1) return FATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H * S > 0x7fffffffLL) return FATTN_ERR_INVALID_ARG;
   const size_t need = fattn_decode_workspace_size(B, H, Nk, d, num_splits);
@@ -442,7 +450,7 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
   if (!(scale > 0.f) || !isfinite(scale)) return FATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
   const size_t cap = FATTN_DECODE_STATIC_WORKSPACE_BYTES;
-  int S = fattn_decode_num_splits(Nk, num_splits);
+  int S = fattn_decode_num_splits(B, H, Nk, num_splits);
   if (S < 1) return FATTN_ERR_INVALID_ARG;
   if (num_splits == 0) {
     // largest split count (at most one per 64-key block) whose partial states fit

@@ -73,6 +73,7 @@ FwdSlot fwd_slot(long long hc, long long Nq, long long Nk, long long d) {
 // ... and of the decode's, for `hc` heads of which only the last `nk` keys are copied.
 struct DecSlot {
   size_t q, k, v, o, lse, ws, ws_bytes, bytes;
+  int splits;  // split count of a full chunk, used for every chunk so that each fits the slot
 };
 DecSlot dec_slot(long long hc, long long nk, int d) {
   DecSlot s;
@@ -82,7 +83,8 @@ DecSlot dec_slot(long long hc, long long nk, int d) {
   s.o = s.v + align256(static_cast<size_t>(hc * nk * d * 2));
   s.lse = s.o + align256(static_cast<size_t>(hc * d * 2));
   s.ws = s.lse + align256(static_cast<size_t>(hc * 4));
-  s.ws_bytes = fattn_decode_workspace_size(1, static_cast<int>(hc), static_cast<int>(nk), d, 0);
+  s.splits = fattn_decode_num_splits(1, static_cast<int>(hc), static_cast<int>(nk), 0);
+  s.ws_bytes = fattn_decode_workspace_size(1, static_cast<int>(hc), static_cast<int>(nk), d, s.splits);
   s.bytes = s.ws + align256(s.ws_bytes);
   return s;
 }
@@ -222,9 +224,8 @@ fattn_status fattn_decode_host(const void* q_host, const void* k_host, const voi
     return e;
   };
   auto compute = [&](char* slot, long long n, cudaStream_t s) {
-    const size_t ws = fattn_decode_workspace_size(1, static_cast<int>(n), nk, d, 0);
     return fattn_decode(slot + sl.q, slot + sl.k, slot + sl.v, slot + sl.o, reinterpret_cast<float*>(slot + sl.lse),
-                        1, static_cast<int>(n), nk, d, scale, 0, slot + sl.ws, ws, s);
+                        1, static_cast<int>(n), nk, d, scale, sl.splits, slot + sl.ws, sl.ws_bytes, s);
   };
   auto copy_out = [&](char* slot, long long bh0, long long n, cudaStream_t s) {
     cudaError_t e = cudaMemcpyAsync(oh + bh0 * qrow, slot + sl.o, n * qrow, cudaMemcpyDeviceToHost, s);

@@ -131,11 +131,14 @@ fattn_status fattn_bwd_masked(const void* q, const void* k, const void* v, const
  * fattn_decode_num_splits -- the number of key splits fattn_decode uses for a request.
  *
  * The cached keys are cut into blocks of 64; nblk = ceil(Nk / 64).  `num_splits` = 0 asks for the
- * default, one partial state per 64-key block (nblk splits).  A value in [1, nblk] is used as given;
- * split s then covers blocks [s*nblk/S, (s+1)*nblk/S).  Returns the resolved count, or -1 if the
- * request is invalid (Nk < 1 or num_splits outside [0, nblk]).
+ * default: splits of about 8 blocks (512 keys), or more of them, up to one per block, while fewer
+ * than 8192 (b, h, split) work items would be left for the GPU:
+ *     S = min(nblk, max(ceil(nblk / 8), ceil(8192 / (B H)))).
+ * A value in [1, nblk] is used as given; split s then covers blocks [s*nblk/S, (s+1)*nblk/S).
+ * Returns the resolved count, or -1 if the request is invalid (B, H or Nk < 1, or num_splits
+ * outside [0, nblk]).
  */
-int fattn_decode_num_splits(int Nk, int num_splits);
+int fattn_decode_num_splits(int B, int H, int Nk, int num_splits);
 
 /*
  * fattn_decode_workspace_size -- bytes of scratch fattn_decode needs for these sizes.
@@ -193,7 +196,7 @@ fattn_status fattn_decode_masked(const void* q, const void* k_cache, const void*
  * of device memory on every GPU that loads the library, held until the process exits).  Nothing is
  * allocated, by this library or by any library it calls.
  *
- *   num_splits  0 picks the largest split count, at most one per 64-key block, whose partial
+ *   num_splits  0 starts from fattn_decode_num_splits's default and lowers it until the partial
  *               states fit in the array; an explicit count must fit in the array too.
  *   Returns FATTN_ERR_INVALID_ARG, launching nothing, when the partial states for these sizes do
  *   not fit (B * H * num_splits * (d + 2) floats, each of the two arrays rounded up to 256 bytes,

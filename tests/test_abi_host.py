@@ -68,20 +68,29 @@ def test_fwd_rejects_bad_arguments(L, args, expect):
 
 
 def test_decode_split_resolution(L):
-    assert L.fattn_decode_num_splits(16384, 0) == 256
-    assert L.fattn_decode_num_splits(65, 0) == 2
-    assert L.fattn_decode_num_splits(1, 0) == 1
-    assert L.fattn_decode_num_splits(1000, 16) == 16
-    assert L.fattn_decode_num_splits(1000, 17) == -1
-    assert L.fattn_decode_num_splits(0, 0) == -1
-    assert L.fattn_decode_num_splits(100, -1) == -1
+    # default: about 8 blocks of 64 keys per split, more splits while B H S < 8192, at most nblk
+    assert L.fattn_decode_num_splits(32, 32, 16384, 0) == 32
+    assert L.fattn_decode_num_splits(8, 32, 16384, 0) == 32
+    assert L.fattn_decode_num_splits(4, 8, 32768, 0) == 256
+    assert L.fattn_decode_num_splits(1, 32, 131072, 0) == 256
+    assert L.fattn_decode_num_splits(1, 1, 16384, 0) == 256
+    assert L.fattn_decode_num_splits(64, 256, 100000, 0) == 196
+    assert L.fattn_decode_num_splits(1, 1, 65, 0) == 2
+    assert L.fattn_decode_num_splits(1, 1, 1, 0) == 1
+    assert L.fattn_decode_num_splits(1, 1, 1000, 16) == 16
+    assert L.fattn_decode_num_splits(1, 1, 1000, 17) == -1
+    assert L.fattn_decode_num_splits(1, 1, 0, 0) == -1
+    assert L.fattn_decode_num_splits(1, 1, 100, -1) == -1
+    assert L.fattn_decode_num_splits(0, 1, 100, 0) == -1
 
 
 def test_decode_workspace_size(L):
     # one fp32 (m, l, O[d]) per (b, h, split), each array padded to 256 bytes
     def pad(x):
         return (x + 255) // 256 * 256
-    assert L.fattn_decode_workspace_size(32, 32, 16384, 128, 0) == pad(32 * 32 * 256 * 128 * 4) + pad(32 * 32 * 256 * 2 * 4)
+    # the default for B32 H32 Nk16384 is 32 splits (8 blocks of 64 keys each)
+    assert L.fattn_decode_workspace_size(32, 32, 16384, 128, 0) == pad(32 * 32 * 32 * 128 * 4) + pad(32 * 32 * 32 * 2 * 4)
+    assert L.fattn_decode_workspace_size(32, 32, 16384, 128, 256) == pad(32 * 32 * 256 * 128 * 4) + pad(32 * 32 * 256 * 2 * 4)
     assert L.fattn_decode_workspace_size(1, 1, 1, 64, 0) == 256 + 256
     assert L.fattn_decode_workspace_size(0, 1, 1, 64, 0) == 0
     assert L.fattn_decode_workspace_size(1, 1, 100, 64, 3) == 0
