@@ -72,6 +72,24 @@ def visible_pairs(N, window_left=-1):
     return W * (W + 1) / 2 + (N - W) * W
 
 
+# ex2 rate of one SM (GB300, measured by a microbenchmark: one warp instruction per 4 cycles per
+# scheduler) and the GB300's maximum SM clock
+EX2_PER_CLOCK_PER_SM = 32
+MAX_SM_HZ = 2070e6
+
+
+def sfu_roofline(P, window_left, ms):
+    """The d = 64 prefill's second bound: one ex2 per visible (query, key) pair against the SFU rate."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    exps = P["B"] * P["H"] * visible_pairs(P["N"], window_left)
+    achieved = exps / (ms * 1e-3) / 1e9
+    peak = EX2_PER_CLOCK_PER_SM * sms * MAX_SM_HZ / 1e9
+    return {"bound": "sfu (ex2)", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "Gexp2/s",
+            "frac": round(achieved / peak, 4), "exp2_per_launch": exps,
+            "peak_source": f"{EX2_PER_CLOCK_PER_SM} ex2 per clock per SM x {sms} SMs x 2070 MHz (maximum SM clock)"}
+
+
 def backward_flops(B, H, N, d, causal):
     # the five products of the backward (S, dP, dV, dK, dQ), 2*N*N*d each; half under the causal mask
     f = 10.0 * B * H * N * N * d
@@ -461,6 +479,7 @@ def run_ours(args):
             "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM)",
             "traffic": recorded_traffic("prefill"),
             "algorithmic_bytes": prefill_bytes(P["B"], P["H"], P["N"], P["d"]),
+            "secondary": sfu_roofline(P, args.window, pre_avg),
         }
     if do_decode:
         dec_bw = decode_bytes(D["B"], D["H"], D["Nk"], D["d"]) / (dec_avg * 1e-3) / 1e9
