@@ -232,15 +232,25 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     for (int h = 0; h < 4; ++h) wait_dep(s[h]);
     const int kv0 = j * kBlockN;
     if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > hi || kv0 < lo)) {
-      // Keys past this row's visible range, as offsets into the tile: one compare with an
-      // immediate per key, and no lower-side compare when the band has no lower bound (causal).
+      // Keys outside this row's visible range, as offsets into the tile: one compare with an
+      // immediate per key and side, and only the sides that cut into this tile for some row of the
+      // warp (a causal diagonal tile or a band's upper edge: the upper side; a band's lower edge:
+      // the lower side).
       const int vhi = hi - kv0, vlo = lo - kv0;
-      if (a.wl < 0) {
+      const bool cut_lo = __any_sync(0xffffffffu, vlo > 0);
+      const bool cut_hi = __any_sync(0xffffffffu, vhi < kBlockN - 1);
+      if (!cut_lo) {
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (32 * h + i > vhi) s[h][i] = __float_as_uint(-INFINITY);
+      } else if (!cut_hi) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
       } else {
 #pragma unroll
         for (int h = 0; h < 4; ++h)
