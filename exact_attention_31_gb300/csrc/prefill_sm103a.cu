@@ -283,6 +283,24 @@ __device__ __noinline__ void recompute_row(const Args& a, int bh, int row, int k
   atomicAdd(a.recomputed, 1ull);
 }
 
+// Max of a row's 128 scores as a balanced tree of three-input maxes: 66 instructions, five deep (the
+// first step of a unit waits on it, so its depth matters more than its count).
+__device__ __forceinline__ float max128_tree(const uint32_t (&s)[4][32]) {
+  auto at = [&](int e) { return __uint_as_float(s[e >> 5][e & 31]); };
+  float a[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) a[i] = max3f(at(3 * i), at(3 * i + 1), at(3 * i + 2));
+  a[42] = fmaxf(at(126), at(127));
+  float b[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) b[i] = max3f(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[14] = a[42];
+  float c5[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) c5[i] = max3f(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+  return fmaxf(max3f(c5[0], c5[1], c5[2]), fmaxf(c5[3], c5[4]));
+}
+
 // ------------------------------------------------------------------------------------------------
 // Softmax group: one thread per query row.
 // ------------------------------------------------------------------------------------------------
@@ -357,21 +375,10 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
             if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
       }
     }
-    // The reference is the max of the row's first key tile that holds a visible key (eight
-    // independent three-input chains); later tiles leave it in place.
+    // The reference is the max of the row's first key tile that holds a visible key; later tiles
+    // leave it in place.
     if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
-      float mx8[8];
-  #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[0][2 * k]), __uint_as_float(s[0][2 * k + 1]));
-  #pragma unroll
-      for (int e = 16; e < 128; e += 16) {
-  #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mx8[k] = max3f(mx8[k], __uint_as_float(s[(e + 2 * k) >> 5][(e + 2 * k) & 31]),
-                         __uint_as_float(s[(e + 2 * k + 1) >> 5][(e + 2 * k + 1) & 31]));
-      }
-      const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), fmaxf(max3f(mx8[3], mx8[4], mx8[5]),
-                                                                  max3f(mx8[6], mx8[7], mx8[7])));
+      const float mx = max128_tree(s);
       if (m_ref == -INFINITY) m_ref = mx * c;
     }
     const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
