@@ -197,6 +197,24 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
+// Max of a row's 128 scores as a balanced tree of three-input maxes: 66 instructions, five deep (every
+// step waits on it before its exponentials).
+__device__ __forceinline__ float max128_tree(const uint32_t (&s)[4][32]) {
+  auto at = [&](int e) { return __uint_as_float(s[e >> 5][e & 31]); };
+  float a[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) a[i] = max3f(at(3 * i), at(3 * i + 1), at(3 * i + 2));
+  a[42] = fmaxf(at(126), at(127));
+  float b[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) b[i] = max3f(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[14] = a[42];
+  float c5[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) c5[i] = max3f(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+  return fmaxf(max3f(c5[0], c5[1], c5[2]), fmaxf(c5[3], c5[4]));
+}
+
 // ------------------------------------------------------------------------------------------------
 // Softmax group: one thread per query row.  g counts tile t's steps over the CTA's units (phases
 // of S_full / P_full); done counts its non-empty units (phases of O_full / O_free).
@@ -259,17 +277,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
             if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
       }
     }
-    float mx8[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[0][2 * k]), __uint_as_float(s[0][2 * k + 1]));
-#pragma unroll
-    for (int e = 16; e < 128; e += 16) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mx8[k] = max3f(mx8[k], __uint_as_float(s[(e + 2 * k) >> 5][(e + 2 * k) & 31]),
-                       __uint_as_float(s[(e + 2 * k + 1) >> 5][(e + 2 * k + 1) & 31]));
-    }
-    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), fmaxf(max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    const float mx = max128_tree(s);
     const float m_new = fmaxf(m_ref, mx * c);
     const bool need = m_new > m_ref + kRescaleLog2;
     float corr = 1.f;
