@@ -89,3 +89,44 @@ def test_backward_from_recomputed_rows(fa):
     for name, a_, b_ in zip(("dq", "dk", "dv"), g_fwd, g_exact):
         a64, b64 = to64(a_), to64(b_)
         assert np.abs(a64 - b64).max() <= 5e-2 * np.abs(b64).max(), name
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_windowed_rows_with_rising_scores(fa, d):
+    # A sliding window of 192 keys: row i sees keys [i - 191, i].  Keys 320..447 are 30 u + noise
+    # (scores near 900), the others N(0, 1).  A row's reference is set by its first key tile with a
+    # visible key, so a row that sees the large keys is recomputed exactly when that first tile
+    # holds none of them: rows 320..446 (their windows start in key tile 1, keys 128..255), 127 per
+    # head; rows 447..511 start in tile 2, which already holds large keys they see.
+    B, H, N = 1, 2, 512
+    g = torch.Generator().manual_seed(4700 + d)
+    u = torch.randn(d, generator=g, dtype=torch.float64)
+    u /= u.norm()
+    q = 30 * u + 0.1 * torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    k = torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    k[:, :, 320:448] = 30 * u + 0.1 * torch.randn(B, H, 128, d, generator=g, dtype=torch.float64)
+    v = torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    q, k, v = (t.to(torch.bfloat16).cuda() for t in (q, k, v))
+    scale = 1.0 / math.sqrt(d)
+    band = (191, 0)
+    before = fa.fattn_fwd_recomputed_rows()
+    o, lse = fa.fattn_fwd(q, k, v, window=band, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    recomputed = fa.fattn_fwd_recomputed_rows() - before
+    expect = 0
+    for i in range(N):
+        lo_k, hi_k = max(i - 191, 0), i
+        sees_big = hi_k >= 320 and lo_k <= 447
+        if not sees_big:
+            continue
+        t0 = lo_k // 128
+        first_tile_keys = range(max(lo_k, 128 * t0), min(hi_k, 128 * t0 + 127) + 1)
+        ref_has_big = any(320 <= j <= 447 for j in first_tile_keys)
+        if not ref_has_big:
+            expect += 1
+    assert recomputed == B * H * expect, (recomputed, B * H * expect)
+    o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), window=band, scale=scale)
+    err = np.abs(to64(o) - o_ref)
+    assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (err.max(), err.mean())
+    assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS * max(1.0, np.abs(lse_ref).max() / 64)
