@@ -132,7 +132,7 @@ def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, or None when the kernel source has
     changed since the counters were taken.  Lines: `<kernel> <source-sha16> <bytes_per_launch>`."""
     src = {"prefill": PREFILL_KERNEL_SRC, "decode": DECODE_KERNEL_SRC, "backward64": BACKWARD_KERNEL_SRC,
-           "backward128": BACKWARD_KERNEL_SRC, "fp8": PREFILL_FP8_KERNEL_SRC}[kernel]
+           "backward128": BACKWARD_KERNEL_SRC, "fp8": PREFILL_FP8_KERNEL_SRC, "fp8_64": PREFILL_FP8_KERNEL_SRC}[kernel]
     try:
         digest = source_digest(src)
         with open(TRAFFIC_FILE) as f:
@@ -615,7 +615,8 @@ def run_backward(args):
 
 
 def run_fp8(args):
-    """Time fattn_fwd_fp8 (V transpose + fused kernel) on B1 H32 N8192 d128 causal with e4m3 inputs.
+    """Time fattn_fwd_fp8 (V transpose + fused kernel) on B1 H32 N8192 causal, d 128 (or --fp8-d 64),
+    with e4m3 inputs.
     A line of its own, outside the benchmark step: the step is the bf16 forward hot path."""
     import torch
     world, rank, local = dist_env()
@@ -625,7 +626,7 @@ def run_fp8(args):
     import exact_attention_31_gb300 as fa
     from exact_attention_31_gb300.workloads import make_qkv_fp8
     fa.lib()
-    B, H, N, d = 1, args.prefill_heads or 32, 8192, 128
+    B, H, N, d = 1, args.prefill_heads or 32, 8192, args.fp8_d or 128
     stream = torch.cuda.current_stream(dev)
     scale = 1 / math.sqrt(d)
     (q, k, v), (qs, ks, vs), _ = make_qkv_fp8(B, H, N, N, d, 0xFA77E000 + 6, dev)
@@ -692,10 +693,11 @@ def run_fp8(args):
                    "l2": "a 512 MiB buffer is written before every call (outside the per-call events)",
                    "parallelism": f"replicas x{world}"},
         "fp8_ms": round(avg, 4),
-        "roofline": {"kernel": "fattn_fwd_fp8 (fwd_fp8_vt_kernel + prefill_fp8_kernel)", "bound": "tensor",
+        "roofline": {"kernel": f"fattn_fwd_fp8 (fwd_fp8_vt_kernel<{d}> + prefill_fp8_kernel<{d}>)", "bound": "tensor",
                      "achieved": round(tf, 2), "peak": fp8_peak, "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
                      "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM) x 2, the nominal fp8:bf16 ratio",
-                     "traffic": recorded_traffic("fp8") if (B, H, N) == (1, 32, 8192) and args.window < 0 else None,
+                     "traffic": recorded_traffic("fp8" if d == 128 else "fp8_64")
+                     if (B, H, N) == (1, 32, 8192) and args.window < 0 else None,
                      "traffic_kernel": "prefill_fp8_kernel alone (ncu)",
                      "algorithmic_bytes": B * H * N * d * 3 + B * H * N * d * 2 + B * H * N * 4},
         "gpu_launches": 2 * args.steps,
@@ -869,6 +871,7 @@ def main(argv=None):
                     help="both = the benchmark step; prefill/decode time one half (profiling); backward "
                          "times fattn_bwd on the prefill shape (a line of its own)")
     ap.add_argument("--bwd-d", type=int, default=0, help="override d of the backward workload (64 or 128)")
+    ap.add_argument("--fp8-d", type=int, default=0, help="d of the fp8 workload (64 or 128; default 128)")
     ap.add_argument("--window", type=int, default=-1,
                     help="sliding-window band (W-1, 0) for the prefill/backward workloads (FLOPs = visible pairs)")
     ap.add_argument("--prefill-heads", type=int, default=0, help="override H of the prefill (profiling)")

@@ -425,7 +425,7 @@ def fattn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float,
                   scale: float | None = None, window=None, out=None, lse=None, workspace=None, stream=None,
                   want_lse: bool = True):
     """Attention of q*q_descale, k*k_descale, v*v_descale (fattn_fwd_fp8): q, k, v are
-    torch.float8_e4m3fn [B,H,N,128] CUDA tensors; out bf16, lse fp32.  ``workspace`` (a CUDA uint8
+    torch.float8_e4m3fn [B,H,N,d] CUDA tensors, d 64 or 128; out bf16, lse fp32.  ``workspace`` (a CUDA uint8
     tensor of fattn_fwd_fp8_workspace_size(...) bytes) receives V transposed; allocated here if
     omitted.  Returns (out, lse)."""
     import torch

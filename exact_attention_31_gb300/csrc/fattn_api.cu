@@ -140,17 +140,20 @@ bool make_map_f32(CUtensorMap* map, void* base, int BH, int rows, int d) {
   return r == CUDA_SUCCESS;
 }
 
-// 3-D byte tensor [BH][rows][cols] (e4m3 operands), 128 x 128 boxes, 128-byte swizzle; out-of-range
-// elements read as zero.  cols and the row pitch are multiples of 16 bytes.
-bool make_map_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols) {
+// 3-D byte tensor [BH][rows][cols] (e4m3 operands), boxes of box_rows rows x box_cols bytes (128 or
+// 64) with the swizzle of the same span; out-of-range elements read as zero.  cols and the row pitch
+// are multiples of 16 bytes.
+bool make_map_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols, int box_cols, int box_rows) {
   EncodeTiledFn fn = encode_tiled();
   if (fn == nullptr) return false;
+  if (box_cols != 128 && box_cols != 64) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows) * cols};
-  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estride[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -370,7 +373,7 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
 extern "C" {
 
 size_t fattn_fwd_fp8_workspace_size(int B, int H, int Nk, int d) {
-  if (!positive_sizes(B, H, Nk, 1) || d != 128) return 0;
+  if (!positive_sizes(B, H, Nk, 1) || (d != 128 && d != 64)) return 0;
   return align_up(static_cast<size_t>(B) * H * d * fp8_padded_keys(Nk), 256);
 }
 
@@ -385,19 +388,20 @@ fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   for (float x : {scale, q_descale, k_descale, v_descale})
     if (!(x > 0.f) || !isfinite(x)) return FATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 0x7fffffffLL / 64 || Nk > 0x7fffffff - 128) return FATTN_ERR_INVALID_ARG;
-  if (d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (d != 128 && d != 64) return FATTN_ERR_UNSUPPORTED;
   const size_t need = fattn_fwd_fp8_workspace_size(B, H, Nk, d);
   if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
   const int BH = B * H;
   const int Nk_pad = fp8_padded_keys(Nk);
   CUtensorMap tq, tk, tvt;
-  if (!make_map_u8(&tq, q, BH, Nq, d) || !make_map_u8(&tk, k, BH, Nk, d) || !make_map_u8(&tvt, workspace, BH, d, Nk_pad))
+  if (!make_map_u8(&tq, q, BH, Nq, d, d, 128) || !make_map_u8(&tk, k, BH, Nk, d, d, 128) ||
+      !make_map_u8(&tvt, workspace, BH, d, Nk_pad, 128, d))
     return FATTN_ERR_CUDA;
   unsigned int* status = nullptr;
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_vt_transpose(v, workspace, BH, Nk, s) != cudaSuccess) return FATTN_ERR_CUDA;
-  Fp8Problem p{q, k, workspace, o, lse, B, H, Nq, Nk, window_left, window_right, scale, q_descale, k_descale,
+  if (launch_vt_transpose(v, workspace, BH, Nk, d, s) != cudaSuccess) return FATTN_ERR_CUDA;
+  Fp8Problem p{q, k, workspace, o, lse, B, H, Nq, Nk, d, window_left, window_right, scale, q_descale, k_descale,
                v_descale, test_drop_kv_block()};
   if (launch_prefill_fp8(p, tq, tk, tvt, status, wait_timeout_ns(), s) != cudaSuccess) return FATTN_ERR_CUDA;
   return FATTN_OK;

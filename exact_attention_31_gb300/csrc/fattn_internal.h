@@ -86,24 +86,24 @@ cudaError_t launch_backward(const BwdProblem& p, const CUtensorMap& tq, const CU
                             const CUtensorMap& tdo, const CUtensorMap& tdq, unsigned int* status,
                             unsigned long long timeout_ns, cudaStream_t stream);
 
-// FP8 forward (d = 128): q, k, v are e4m3 [B*H][N][128]; the attention is that of q * q_descale,
-// k * k_descale, v * v_descale.  vt is V transposed, [B*H][128][fp8_padded_keys(Nk)].
+// FP8 forward (d = 64 or 128): q, k, v are e4m3 [B*H][N][d]; the attention is that of q * q_descale,
+// k * k_descale, v * v_descale.  vt is V transposed, [B*H][d][fp8_padded_keys(Nk)].
 struct Fp8Problem {
   const void* q;
   const void* k;
   const void* vt;
   void* o;
   float* lse;
-  int B, H, Nq, Nk;
+  int B, H, Nq, Nk, d;
   int window_left, window_right;
   float scale, q_descale, k_descale, v_descale;
   int drop_kv_block;  // failure-detection testing only: key tile never loaded (-1 = off)
 };
 
 int fp8_padded_keys(int Nk);
-cudaError_t launch_vt_transpose(const void* v, void* vt, int BH, int Nk, cudaStream_t stream);
-// tq, tk: [B*H][N][128] e4m3, 128 x 128 boxes; tvt: [B*H][128][Nk_pad] e4m3, 128 x 128 boxes;
-// all with 128-byte swizzle.
+cudaError_t launch_vt_transpose(const void* v, void* vt, int BH, int Nk, int d, cudaStream_t stream);
+// tq, tk: [B*H][N][d] e4m3, d x 128-row boxes (128-byte swizzle for d = 128, 64-byte for d = 64);
+// tvt: [B*H][d][Nk_pad] e4m3, 128-key x d-row boxes, 128-byte swizzle.
 cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tvt, unsigned int* status, unsigned long long timeout_ns,
                                cudaStream_t stream);

@@ -1,4 +1,4 @@
-// prefill_fp8_sm103a.cu -- fused exact attention forward on FP8 (e4m3) operands, d = 128, sm_103a.
+// prefill_fp8_sm103a.cu -- fused exact attention forward on FP8 (e4m3) operands, d = 64 or 128, sm_103a.
 //
 // The computation is the same tiled online-softmax forward as the bf16 kernel ("Flash Attention:
 // The Hidden Gem", The Algorithm; "FlashAttention: attention was never compute-bound", The one
@@ -9,7 +9,9 @@
 //   S_t = Q_t K_j^T    A = Q_t (smem, K-major), B = K_j (smem, K-major), 32 elements per K step
 //   O_t += P_t V_j     A = P_t in TMEM as e4m3 (four keys per 32-bit column), B = V_j^T (smem, K-major)
 // 8-bit operands are read K-major only, so V is transposed once per call into a workspace
-// ([B*H][d][Nk rounded up to 16] e4m3, keys past Nk zero) by fwd_fp8_vt_kernel.
+// ([B*H][d][Nk rounded up to 16] e4m3, keys past Nk zero) by fwd_fp8_vt_kernel.  A Q or K tile is
+// 128 rows of d bytes: with d = 128 it is stored with the 128-byte swizzle, with d = 64 with the
+// 64-byte one (a row is one 64-byte swizzle span).  A V^T tile is d rows of 128 keys, 128-byte swizzle.
 //
 // Layout per CTA (persistent, one per SM, 320 threads): warps 0-3 and 4-7 the softmax of two
 // 128-row query tiles (one thread per row), warp 8 the TMA producer, warp 9 the MMA issuer and TMEM
@@ -31,7 +33,6 @@
 namespace fattn {
 namespace {
 
-constexpr int kD = 128;
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kTiles = 2;
@@ -41,13 +42,9 @@ constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 3.0f;
 constexpr float kPScaleLog2 = 5.0f;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTileBytes = kBlockM * kD;  // one 128 x 128 e4m3 tile (also V^T: 128 rows of 128 keys)
-constexpr int kSlots = 8;                      // K/V^T ring
+constexpr int kSlots = 8;  // K/V^T ring
 
 struct F8Cfg {
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKVOff = kQOff + kTiles * kTileBytes;
-  static constexpr uint32_t kBarOff = kKVOff + kSlots * kTileBytes;
   static constexpr int kQFull = 0;     // [2]
   static constexpr int kSFull = 2;     // [2]
   static constexpr int kPFull = 4;     // [2] one arrival per softmax warp
@@ -58,12 +55,22 @@ struct F8Cfg {
   static constexpr int kKVFull = 13;   // [kSlots]
   static constexpr int kKVEmpty = 13 + kSlots;
   static constexpr int kNumBars = 13 + 2 * kSlots;
-  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 };
 using C = F8Cfg;
+
+// Shared memory of the head dimension D: two Q tiles, then the K/V^T ring, then the barriers.
+template <int D>
+struct F8Smem {
+  static constexpr uint32_t kTileBytes = kBlockM * D;  // a Q or K tile (128 x D), or a V^T tile (D x 128)
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKVOff = kQOff + kTiles * kTileBytes;
+  static constexpr uint32_t kBarOff = kKVOff + kSlots * kTileBytes;
+  static constexpr uint32_t kMiscOff = kBarOff + C::kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+  static_assert(kTileBytes % 1024 == 0, "tiles stay on 1024-byte swizzle-atom boundaries");
+};
 
 struct F8Args {
   __nv_bfloat16* o;
@@ -219,6 +226,7 @@ __device__ __forceinline__ float max128_tree(const uint32_t (&s)[4][32]) {
 // Softmax group: one thread per query row.  g counts tile t's steps over the CTA's units (phases
 // of S_full / P_full); done counts its non-empty units (phases of O_full / O_free).
 // ------------------------------------------------------------------------------------------------
+template <int D>
 __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
                                              uint32_t sbar, const F8Args& a, const Abort& ab, int& g, int& done) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,7 +317,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
     if (step > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-      for (int h = 0; h < kD / 32; ++h) {
+      for (int h = 0; h < D / 32; ++h) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tO + 32 * h, o);
         wait_dep(o);
@@ -330,12 +338,12 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   }
   if (!ok) return false;
   const bool store = q_row < a.Nq;
-  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * kD;
+  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
   if (n_tiles == 0) {
     if (store) {
       uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int i = 0; i < kD / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       if (a.lse != nullptr) a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = -INFINITY;
     }
     return true;
@@ -344,7 +352,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   tc_fence_after();
   const float f = l > 0.f ? a.v_descale / l : 0.f;
 #pragma unroll
-  for (int h = 0; h < kD / 32; ++h) {
+  for (int h = 0; h < D / 32; ++h) {
     uint32_t o[32];
     tmem_ld_32x32b_x32(tO + 32 * h, o);
     wait_dep(o);
@@ -367,21 +375,24 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   return true;
 }
 
+template <int D>
 __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbar, const F8Args& a, Abort ab) {
   int g = 0, done = 0;
   Unit u;
   for (int k = 0; cta_unit(k, a, u); ++k) {
     ab.renew(a.timeout_ns);
-    if (!softmax_unit(t, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done)) return;
+    if (!softmax_unit<D>(t, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done)) return;
   }
 }
 
 // ------------------------------------------------------------------------------------------------
 // TMA producer (one thread): Q tiles once per unit, then K_j and V_j^T through the ring.
 // ------------------------------------------------------------------------------------------------
+template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tvt,
                                               uint32_t sbase, const F8Args& a, Abort ab) {
-  const uint32_t sbar = sbase + C::kBarOff;
+  using M = F8Smem<D>;
+  const uint32_t sbar = sbase + M::kBarOff;
   tma_prefetch_desc(tq);
   tma_prefetch_desc(tk);
   tma_prefetch_desc(tvt);
@@ -400,8 +411,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
         break;
       }
       const uint32_t bar = sbar + 8 * (C::kQFull + t);
-      mbar_arrive_expect_tx(bar, kTileBytes);
-      tma_load_3d(sbase + C::kQOff + t * kTileBytes, tq, bar, 0, u.row0 + t * kBlockM, u.bh);
+      mbar_arrive_expect_tx(bar, M::kTileBytes);
+      tma_load_3d(sbase + M::kQOff + t * M::kTileBytes, tq, bar, 0, u.row0 + t * kBlockM, u.bh);
       ++qloads[t];
     }
     if (!ok) break;
@@ -421,8 +432,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
           continue;
         }
         const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
-        mbar_arrive_expect_tx(bar, kTileBytes);
-        const uint32_t dst = sbase + C::kKVOff + slot * kTileBytes;
+        mbar_arrive_expect_tx(bar, M::kTileBytes);
+        const uint32_t dst = sbase + M::kKVOff + slot * M::kTileBytes;
         if (w == 0) tma_load_3d(dst, tk, bar, 0, j * kBlockN, u.bh);   // K_j: 128 keys x d
         else tma_load_3d(dst, tvt, bar, j * kBlockN, 0, u.bh);         // V_j^T: d rows x 128 keys
         issued = idx + 1;
@@ -464,31 +475,44 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// K-major descriptor of a Q or K tile (128 rows of D bytes): 128-byte swizzle with 1024-byte atoms
+// for D = 128, 64-byte swizzle with 512-byte atoms for D = 64.
+template <int D>
+__device__ __forceinline__ uint64_t qk_desc(uint32_t addr) {
+  if constexpr (D == 128) return smem_desc_sw128(addr, 16, 1024);
+  else return smem_desc_sw64(addr);
+}
+
+template <int D>
 struct MmaCtx {
+  using M = F8Smem<D>;
   uint32_t tmem, sbar, lead;
-  uint64_t dq[kTiles], dkv0;
+  uint64_t dq[kTiles], dk0, dv0;
   __device__ __forceinline__ void init(uint32_t tmem_, uint32_t sbase) {
     tmem = tmem_;
-    sbar = sbase + C::kBarOff;
+    sbar = sbase + M::kBarOff;
 #pragma unroll
-    for (int t = 0; t < kTiles; ++t) dq[t] = smem_desc_sw128(sbase + C::kQOff + t * kTileBytes, 16, 1024);
-    dkv0 = smem_desc_sw128(sbase + C::kKVOff, 16, 1024);
+    for (int t = 0; t < kTiles; ++t) dq[t] = qk_desc<D>(sbase + M::kQOff + t * M::kTileBytes);
+    dk0 = qk_desc<D>(sbase + M::kKVOff);
+    dv0 = smem_desc_sw128(sbase + M::kKVOff, 16, 1024);
     lead = elect_lane();
   }
-  __device__ __forceinline__ static uint64_t slot_adv(int slot) { return static_cast<uint64_t>(slot) * (kTileBytes >> 4); }
-  // S_t = Q_t K^T: four K steps of 32 e4m3 (32 bytes) along d
+  __device__ __forceinline__ static uint64_t slot_adv(int slot) {
+    return static_cast<uint64_t>(slot) * (M::kTileBytes >> 4);
+  }
+  // S_t = Q_t K^T: D / 32 K steps of 32 e4m3 (32 bytes) along d
   __device__ __forceinline__ void issue_s(int t, int slot) const {
     constexpr uint32_t id = idesc_e4m3(kBlockM, kBlockN);
 #pragma unroll
-    for (int kk = 0; kk < kD / 32; ++kk)
-      mma_f8_ss(tmem + C::col_s(t), dq[t] + 2 * kk, dkv0 + slot_adv(slot) + 2 * kk, id, kk > 0 ? 1u : 0u, lead);
+    for (int kk = 0; kk < D / 32; ++kk)
+      mma_f8_ss(tmem + C::col_s(t), dq[t] + 2 * kk, dk0 + slot_adv(slot) + 2 * kk, id, kk > 0 ? 1u : 0u, lead);
   }
   // O_t += P_t V: four K steps of 32 keys; P_t's 32 keys of a step are 8 TMEM columns
   __device__ __forceinline__ void issue_pv(int t, int slot, bool first) const {
-    constexpr uint32_t id = idesc_e4m3(kBlockM, kD);
+    constexpr uint32_t id = idesc_e4m3(kBlockM, D);
 #pragma unroll
     for (int kk = 0; kk < kBlockN / 32; ++kk)
-      mma_f8_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * kk, dkv0 + slot_adv(slot) + 2 * kk, id,
+      mma_f8_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * kk, dv0 + slot_adv(slot) + 2 * kk, id,
                 (!first || kk > 0) ? 1u : 0u, lead);
   }
   __device__ __forceinline__ void commit(int bar) const { mma_commit_lead(sbar + 8 * bar, lead); }
@@ -507,7 +531,8 @@ struct MmaState {
 
 // Unit schedule: for j = J0 .. J1, first P_t(j-1) V_{j-1}, then S_t(j), per tile; K_j's slot is
 // released after the S(j), V_{j-1}'s after the P V(j-1).  Ring index of K_j is ring + 2 (j - J0).
-__device__ __forceinline__ bool mma_unit(const Unit& u, const MmaCtx& m, MmaState& st, const Abort& ab) {
+template <int D>
+__device__ __forceinline__ bool mma_unit(const Unit& u, const MmaCtx<D>& m, MmaState& st, const Abort& ab) {
   const int J0 = union_begin(u), J1 = union_end(u);
   if (J0 >= J1) return true;
   auto active = [&](int t, int j) { return u.jb[t] <= j && j < u.je[t]; };
@@ -544,8 +569,9 @@ __device__ __forceinline__ bool mma_unit(const Unit& u, const MmaCtx& m, MmaStat
   return true;
 }
 
+template <int D>
 __device__ __forceinline__ void mma_role(uint32_t tmem, uint32_t sbase, const F8Args& a, Abort ab) {
-  MmaCtx m;
+  MmaCtx<D> m;
   m.init(tmem, sbase);
   MmaState st;
   bool ok = true;
@@ -564,6 +590,7 @@ __device__ __forceinline__ void mma_role(uint32_t tmem, uint32_t sbase, const F8
   __syncwarp();
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_vt, const F8Args a) {
@@ -571,9 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
-  const uint32_t sbar = sbase + C::kBarOff;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  using M = F8Smem<D>;
+  const uint32_t sbar = sbase + M::kBarOff;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + M::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + M::kMiscOff + 4);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int t = 0; t < kTiles; ++t) {
@@ -602,12 +630,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   Abort ab{abort_flag, a.status, globaltimer_ns() + a.timeout_ns};
   if (warp < 8) {
-    softmax_role(warp >> 2, tmem, sbar, a, ab);
+    softmax_role<D>(warp >> 2, tmem, sbar, a, ab);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role(&tm_q, &tm_k, &tm_vt, sbase, a, ab);
+    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_vt, sbase, a, ab);
     __syncwarp();
   } else {
-    mma_role(tmem, sbase, a, ab);
+    mma_role<D>(tmem, sbase, a, ab);
   }
   tc_fence_before();
   __syncthreads();
@@ -617,28 +645,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// V [BH][Nk][128] -> V^T [BH][128][Nk_pad] (e4m3 bytes), keys Nk .. Nk_pad - 1 written as zero.
-// One block per (128-key tile, head): the tile is read with 16-byte loads into shared memory; thread
-// (key block kb of 16 keys, word w = 4 d values) reads its 16 words (conflict-free: a warp reads 32
-// words of one row), transposes four 4 x 4 byte blocks with byte permutes, and writes 16 keys of
-// each of its 4 d rows as one 16-byte store.
-__global__ void __launch_bounds__(256) fwd_fp8_vt_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
-                                                         int Nk, int Nk_pad) {
-  __shared__ uint32_t tile[128][33];  // [key][d / 4], padded
+// V [BH][Nk][D] -> V^T [BH][D][Nk_pad] (e4m3 bytes), keys Nk .. Nk_pad - 1 written as zero.
+// One block of 2 D threads per (128-key tile, head): the tile is read with 16-byte loads into shared
+// memory; thread (key block kb of 16 keys, word w = 4 d values) reads its 16 words (conflict-free:
+// the D / 4 words of a row, and for D = 64 two rows 16 banks apart, per warp), transposes four 4 x 4
+// byte blocks with byte permutes, and writes 16 keys of each of its 4 d rows as one 16-byte store.
+template <int D>
+__global__ void __launch_bounds__(2 * D) fwd_fp8_vt_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+                                                           int Nk, int Nk_pad) {
+  constexpr int kWords = D / 4;                // 32-bit words of a key row
+  __shared__ uint32_t tile[128][kWords + 1];  // [key][d / 4], padded
   const int kt = blockIdx.x, bh = blockIdx.y;
   const int key0 = kt * 128;
-  const uint8_t* src = v + static_cast<size_t>(bh) * Nk * kD;
-  for (int i = threadIdx.x; i < 128 * 8; i += 256) {
-    const int key = i >> 3, c = i & 7;  // 16-byte chunk c of row key
+  const uint8_t* src = v + static_cast<size_t>(bh) * Nk * D;
+  for (int i = threadIdx.x; i < 128 * (D / 16); i += 2 * D) {
+    const int key = i / (D / 16), c = i % (D / 16);  // 16-byte chunk c of row key
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (key0 + key < Nk) w = reinterpret_cast<const uint4*>(src + static_cast<size_t>(key0 + key) * kD)[c];
+    if (key0 + key < Nk) w = reinterpret_cast<const uint4*>(src + static_cast<size_t>(key0 + key) * D)[c];
     tile[key][4 * c] = w.x;
     tile[key][4 * c + 1] = w.y;
     tile[key][4 * c + 2] = w.z;
     tile[key][4 * c + 3] = w.w;
   }
   __syncthreads();
-  const int w = threadIdx.x & 31, kb = threadIdx.x >> 5;  // d values 4w .. 4w + 3, keys 16kb .. 16kb + 15
+  const int w = threadIdx.x % kWords, kb = threadIdx.x / kWords;  // d values 4w .. 4w + 3, keys 16kb .. 16kb + 15
   if (key0 + 16 * kb >= Nk_pad) return;
   uint32_t out[4][4];  // [d row r][word: 4 keys]
 #pragma unroll
@@ -652,7 +682,7 @@ __global__ void __launch_bounds__(256) fwd_fp8_vt_kernel(const uint8_t* __restri
     out[2][b4] = __byte_perm(t1, t3, 0x5410);
     out[3][b4] = __byte_perm(t1, t3, 0x7632);
   }
-  uint8_t* dst = vt + static_cast<size_t>(bh) * kD * Nk_pad + key0 + 16 * kb;
+  uint8_t* dst = vt + static_cast<size_t>(bh) * D * Nk_pad + key0 + 16 * kb;
 #pragma unroll
   for (int r = 0; r < 4; ++r)
     *reinterpret_cast<uint4*>(dst + static_cast<size_t>(4 * w + r) * Nk_pad) =
@@ -663,16 +693,21 @@ __global__ void __launch_bounds__(256) fwd_fp8_vt_kernel(const uint8_t* __restri
 
 int fp8_padded_keys(int Nk) { return (Nk + 15) / 16 * 16; }
 
-cudaError_t launch_vt_transpose(const void* v, void* vt, int BH, int Nk, cudaStream_t stream) {
+cudaError_t launch_vt_transpose(const void* v, void* vt, int BH, int Nk, int d, cudaStream_t stream) {
   const int Nk_pad = fp8_padded_keys(Nk);
   dim3 grid(static_cast<unsigned int>((Nk_pad + 127) / 128), static_cast<unsigned int>(BH));
-  fwd_fp8_vt_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), Nk, Nk_pad);
+  const uint8_t* src = static_cast<const uint8_t*>(v);
+  uint8_t* dst = static_cast<uint8_t*>(vt);
+  if (d == 128) fwd_fp8_vt_kernel<128><<<grid, 256, 0, stream>>>(src, dst, Nk, Nk_pad);
+  else if (d == 64) fwd_fp8_vt_kernel<64><<<grid, 128, 0, stream>>>(src, dst, Nk, Nk_pad);
+  else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                               const CUtensorMap& tvt, unsigned int* status, unsigned long long timeout_ns,
-                               cudaStream_t stream) {
+namespace {
+template <int D>
+cudaError_t launch_fp8_d(const F8Args& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                         cudaStream_t stream) {
   static bool attr_set[64] = {};
   static int sm_count[64] = {};
   int dev = 0;
@@ -680,8 +715,8 @@ cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::kSmemBytes));
+    e = cudaFuncSetAttribute(prefill_fp8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(F8Smem<D>::kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -689,6 +724,15 @@ cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
+  const unsigned int grid = static_cast<unsigned int>(min(a.total_units, sm_count[dev]));
+  prefill_fp8_kernel<D><<<grid, kThreads, F8Smem<D>::kSmemBytes, stream>>>(tq, tk, tvt, a);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tvt, unsigned int* status, unsigned long long timeout_ns,
+                               cudaStream_t stream) {
   F8Args a;
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.lse = p.lse;
@@ -705,9 +749,9 @@ cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const
   a.status = status;
   a.timeout_ns = timeout_ns;
   a.drop_kv_block = p.drop_kv_block;
-  const unsigned int grid = static_cast<unsigned int>(min(a.total_units, sm_count[dev]));
-  prefill_fp8_kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tvt, a);
-  return cudaGetLastError();
+  if (p.d == 128) return launch_fp8_d<128>(a, tq, tk, tvt, stream);
+  if (p.d == 64) return launch_fp8_d<64>(a, tq, tk, tvt, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fattn

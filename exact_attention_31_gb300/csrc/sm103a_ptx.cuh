@@ -226,6 +226,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
   return d;
 }
 
+// Descriptor for a K-major operand with 64-byte swizzle: rows of 64 bytes (64 e4m3, two K steps of
+// kind::f8f6f4), 8-row atoms of 512 bytes stacked along M/N; the atom must start on a 512-byte boundary.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;    // leading byte offset (unused: K fits in one swizzle span)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;
+  d |= 1ull << 46;
+  d |= 4ull << 61;  // 64-byte swizzle
+  return d;
+}
+
 // Descriptor for a K-major operand with 32-byte swizzle: rows of 32 bytes (16 bf16, one K step),
 // 8-row atoms of 256 bytes stacked along M/N.
 __device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr) {

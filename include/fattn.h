@@ -226,7 +226,7 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
  *   q_descale, k_descale, v_descale   finite, > 0: the call computes the attention of the dequantised
  *            tensors q * q_descale, k * k_descale, v * v_descale, with the band of fattn_fwd_masked
  *            and the given scale
- *   d        128 only (FATTN_ERR_UNSUPPORTED otherwise)
+ *   d        64 or 128 (FATTN_ERR_UNSUPPORTED otherwise)
  *   workspace  device memory of at least fattn_fwd_fp8_workspace_size(B, H, Nk, d) bytes, 256-byte
  *            aligned, owned by the caller: it receives V transposed ([B*H][d][Nk rounded up to 16]),
  *            because 8-bit operands are read by the tensor core with the reduced dimension contiguous.

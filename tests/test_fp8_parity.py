@@ -76,12 +76,13 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}h{}q{}k{}w{}_{}".format(*c[:4], *c[4]))
-def test_fp8_forward_within_stated_bound(fa, case):
+def test_fp8_forward_within_stated_bound(fa, case, d):
     from exact_attention_31_gb300.workloads import make_qkv_fp8
     B, H, Nq, Nk, band = case
-    (q8, k8, v8), (qs, ks, vs), boosted = make_qkv_fp8(B, H, Nq, Nk, 128, 9000 + Nq + Nk + band[0], device="cuda")
-    scale = 1.0 / math.sqrt(128)
+    (q8, k8, v8), (qs, ks, vs), boosted = make_qkv_fp8(B, H, Nq, Nk, d, 9000 + Nq + Nk + band[0] + d, device="cuda")
+    scale = 1.0 / math.sqrt(d)
     o, lse = fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, window=band, scale=scale)
     torch.cuda.synchronize()
     assert fa.fattn_last_error() == 0
@@ -105,12 +106,30 @@ def test_fp8_b4h16_n2048_boosted_rows_sampled(fa, causal):
     check_bound(o, lse, _deq(q8, qs), _deq(k8, ks), _deq(v8, vs), band, scale, rows=rows, what=f"causal={causal}")
 
 
-def test_fp8_descales_enter_exactly(fa):
+def test_fp8_b1h32_n8192_d64_causal_sampled(fa):
+    # The d = 64 long-sequence configuration (B1 H32 N8192 causal) in e4m3, 1 % of query rows scaled x8;
+    # sampled rows of four heads (the first and last rows of every 256-row unit among them) and
+    # every boosted row of the first head.
+    from exact_attention_31_gb300.workloads import make_qkv_fp8
+    B, H, N, d = 1, 32, 8192, 64
+    (q8, k8, v8), (qs, ks, vs), boosted = make_qkv_fp8(B, H, N, N, d, 9150, device="cuda", boost_frac=0.01)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    per_head = np.unique(np.concatenate([np.arange(0, N, 331), np.arange(0, N, 256), np.arange(255, N, 256)]))
+    rows = [bh * N + per_head for bh in (0, 9, 22, 31)] + [boosted[0].cpu().numpy()]
+    rows = np.unique(np.concatenate(rows))
+    check_bound(o, lse, _deq(q8, qs), _deq(k8, ks), _deq(v8, vs), (-1, 0), scale, rows=rows, what="d64 N8192")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_descales_enter_exactly(fa, d):
     # Doubling v_descale doubles O exactly (it multiplies the fp32 normaliser), and moving a factor 2
     # from scale to q_descale leaves the exponent's fp32 coefficient, and so every output, unchanged.
     from exact_attention_31_gb300.workloads import make_qkv_fp8
-    (q8, k8, v8), (qs, ks, vs), boosted = make_qkv_fp8(1, 2, 256, 256, 128, 9200, device="cuda")
-    sc = 1.0 / math.sqrt(128)
+    (q8, k8, v8), (qs, ks, vs), boosted = make_qkv_fp8(1, 2, 256, 256, d, 9200 + d, device="cuda")
+    sc = 1.0 / math.sqrt(d)
     o1, l1 = fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, scale=sc)
     o2, l2 = fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, 2 * vs, causal=True, scale=sc)
     o3, l3 = fa.fattn_fwd_fp8(q8, k8, v8, 2 * qs, ks, vs, causal=True, scale=sc / 2)
@@ -120,7 +139,7 @@ def test_fp8_descales_enter_exactly(fa):
 
 
 def test_fp8_rejects_other_head_dims(fa):
-    q = torch.zeros((1, 1, 64, 64), dtype=torch.float8_e4m3fn, device="cuda")
+    q = torch.zeros((1, 1, 64, 96), dtype=torch.float8_e4m3fn, device="cuda")
     with pytest.raises(fa.FattnError) as e:
         fa.fattn_fwd_fp8(q, q, q, 1.0, 1.0, 1.0, workspace=torch.empty(4096, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 2
@@ -139,12 +158,13 @@ def _random_cases(n=12, seed=0xF8):
     return out
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "b{}h{}q{}k{}w{}_{}".format(*c[:4], *c[4]))
-def test_fp8_random_shapes_within_stated_bound(fa, case):
+def test_fp8_random_shapes_within_stated_bound(fa, case, d):
     from exact_attention_31_gb300.workloads import make_qkv_fp8
     B, H, Nq, Nk, band = case
-    (q8, k8, v8), (qs, ks, vs), _ = make_qkv_fp8(B, H, Nq, Nk, 128, 9300 + 3 * Nq + Nk, device="cuda")
-    scale = 0.9 / math.sqrt(128)
+    (q8, k8, v8), (qs, ks, vs), _ = make_qkv_fp8(B, H, Nq, Nk, d, 9300 + 3 * Nq + Nk + d, device="cuda")
+    scale = 0.9 / math.sqrt(d)
     o, lse = fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, window=band, scale=scale)
     torch.cuda.synchronize()
     assert fa.fattn_last_error() == 0
