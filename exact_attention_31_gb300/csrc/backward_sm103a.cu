@@ -131,6 +131,8 @@ __host__ __device__ constexpr uint32_t p_col(int half, int chunk) {
 // ... and 16 queries (K step kk of dV += P^T dO) start at this column.
 __host__ __device__ constexpr uint32_t p_step_col(int kk) { return kk < 4 ? 8u * kk : 96u + 8u * (kk - 4); }
 
+constexpr long long kL2GroupBytes = 64ll << 20;
+
 struct BArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -143,6 +145,8 @@ struct BArgs {
   unsigned int* status;
   unsigned long long timeout_ns;
   int drop_kv;  // failure-detection testing only: K_j and V_j are never loaded
+  int nkt;      // key tiles per head
+  int group;    // heads per CTA group (1 .. BH)
 };
 
 struct Abort {
@@ -641,9 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5;
 
-  // Key tiles with the most query tiles (the first ones, under a causal mask) are launched first.
-  const int jt = static_cast<int>(blockIdx.x) / a.BH;
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  // CTAs walk the heads in groups of a.group, sized so that a group's Q, dO and fp32 dQ accumulator
+  // stay in L2; within a group, key tiles with the most query tiles (the first ones, under a causal
+  // mask) are launched first.
+  const int blk = static_cast<int>(blockIdx.x);
+  const int g0 = blk / (a.group * a.nkt) * a.group;
+  const int gsz = min(a.group, a.BH - g0);
+  const int within = blk - g0 * a.nkt;
+  const int jt = within / gsz;
+  const int bh = g0 + within % gsz;
   const int n0 = jt * kBN;
   // Query tiles holding a query that sees any of keys [n0, n0 + 128): q in
   // [n0 - off - wr, k_last - off + wl] clipped to [0, Nq).  None (n = 0) is possible with a band.
@@ -860,7 +870,14 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
   a.status = status;
   a.timeout_ns = timeout_ns;
   a.drop_kv = p.drop_kv;
-  const unsigned int grid = static_cast<unsigned int>((p.Nk + kBN - 1) / kBN) * static_cast<unsigned int>(BH);
+  a.nkt = (p.Nk + kBN - 1) / kBN;
+  {
+    // Heads per group: as many as keep Q, dO (bf16) and the dQ accumulator (fp32) of the group within
+    // 64 MiB, about half of L2 (B1 H32 N8192: 16 heads at d = 64, 8 at d = 128).
+    const long long per_head = static_cast<long long>(Nq_pad) * D * 8;
+    a.group = static_cast<int>(std::max(1LL, std::min<long long>(BH, kL2GroupBytes / per_head)));
+  }
+  const unsigned int grid = static_cast<unsigned int>(a.nkt) * static_cast<unsigned int>(BH);
   bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

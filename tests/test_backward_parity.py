@@ -151,3 +151,21 @@ def test_backward_workload_sampled(fa):
     ref = oracle.attention_backward(to64(pick(q)), to64(pick(k)), to64(pick(v)), to64(pick(do)), causal=True,
                                     scale=w.scale)
     compare_grads((pick(dq), pick(dk), pick(dv)), ref, what="workload heads 0 and 31")
+
+
+def test_backward_partial_head_group_sampled(fa):
+    # B1 H12 N8192 d128 causal: the backward's CTAs walk the heads in groups sized to stay in L2 (8
+    # heads here), so the last group holds 4; heads 0 and 11 (first of the first group, last of the
+    # partial one) are checked whole against the oracle.
+    B, H, N, d = 1, 12, 8192, 128
+    q, k, v, do = _inputs(B, H, N, N, d, seed=3400)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.fattn_bwd(q, k, v, o, lse, do, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    heads = torch.tensor([0, 11], device="cuda")
+    pick = lambda t: t.index_select(1, heads)  # noqa: E731
+    ref = oracle.attention_backward(to64(pick(q)), to64(pick(k)), to64(pick(v)), to64(pick(do)), causal=True,
+                                    scale=scale)
+    compare_grads((pick(dq), pick(dk), pick(dv)), ref, what="B1 H12 N8192 d128 heads 0 and 11")
