@@ -413,12 +413,12 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
       ok = false;
       break;
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(sbar + 8 * (C::kPFull + t));
+    // The row sum is not needed by the hand-off: P_t goes to the MMA warp first.
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
   }
   if (!ok) return false;
   const bool store = q_row < a.Nq;
@@ -438,7 +438,8 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   tc_fence_after();
   // A row that saw no key has l = 0 and m = -inf: o = 0 and L = -inf.
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  float fin = 0.f;  // sum of the outputs / 256: not finite iff one of them is not
+  // Sum of the outputs / 256 (not finite iff one of them is not), in four independent partial sums.
+  float fin = 0.f, fin1 = 0.f, fin2 = 0.f, fin3 = 0.f;
 #pragma unroll
   for (int h = 0; h < D / 32; ++h) {
     uint32_t o[32];
@@ -448,7 +449,13 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float y0 = __uint_as_float(o[2 * i]) * inv_l, y1 = __uint_as_float(o[2 * i + 1]) * inv_l;
-      fin = fmaf(y0, 0x1p-8f, fmaf(y1, 0x1p-8f, fin));
+      if (i & 1) {
+        fin2 = fmaf(y0, 0x1p-8f, fin2);
+        fin3 = fmaf(y1, 0x1p-8f, fin3);
+      } else {
+        fin = fmaf(y0, 0x1p-8f, fin);
+        fin1 = fmaf(y1, 0x1p-8f, fin1);
+      }
       pk[i] = pack_bf16x2(y0, y1);
     }
     if (store) {
@@ -457,6 +464,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
       for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     }
   }
+  fin = (fin + fin1) + (fin2 + fin3);
   // O_t has been read: the next unit's first P_t V may overwrite it.
   tc_fence_before();
   __syncwarp();
