@@ -101,7 +101,8 @@ import exact_attention_31_gb300 as fa
 from exact_attention_31_gb300.workloads import make_qkv, make_qkv_fp8
 from parity_utils import compare, oracle_full
 
-(q8, k8, v8), (qs, ks, vs), _ = make_qkv_fp8(1, 2, 512, 512, 128, seed=11, device="cuda")
+d = int(sys.argv[2])
+(q8, k8, v8), (qs, ks, vs), _ = make_qkv_fp8(1, 2, 512, 512, d, seed=11, device="cuda")
 fa.fattn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)   # key tile 1 is never loaded
 torch.cuda.synchronize()
 assert fa.fattn_last_error() == fa.FATTN_ERR_TIMEOUT
@@ -118,9 +119,10 @@ print("FAILURE-DETECTION-FP8-OK")
 
 
 @pytest.mark.gpu
-def test_fp8_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_bounded_wait_reports_timeout_and_context_survives(d):
     env = dict(os.environ, FATTN_WAIT_TIMEOUT_MS="200", FATTN_TEST_DROP_KV_BLOCK="1")
-    r = subprocess.run([sys.executable, "-c", CHILD_FP8, ROOT], env=env, capture_output=True, text=True,
+    r = subprocess.run([sys.executable, "-c", CHILD_FP8, ROOT, str(d)], env=env, capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "FAILURE-DETECTION-FP8-OK" in r.stdout
