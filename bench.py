@@ -51,14 +51,18 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 # ------------------------------------------------------------------------------------------------
 # Algorithmic work per launch
 # ------------------------------------------------------------------------------------------------
+# The counting rules of the page's traffic counter ("FlashAttention: attention was never
+# compute-bound"), pinned against its printed tables in tests/test_traffic_model.py.
+from exact_attention_31_gb300 import traffic  # noqa: E402
+
+
 def prefill_flops(B, H, N, d, causal):
-    f = 4.0 * B * H * N * N * d
-    return f / 2 if causal else f
+    return traffic.forward_flops(B, H, N, N, d, causal)
 
 
 def prefill_bytes(B, H, N, d):
-    # read Q, K, V once, write O (bf16) and L (fp32)
-    return B * H * N * d * 2 * 4 + B * H * N * 4
+    # read Q, K, V once, write O (bf16) and L (fp32): the tiled count with one query tile per head
+    return traffic.fused_forward_bytes(B, H, N, N, d)
 
 
 def visible_pairs(N, window_left=-1):
@@ -98,16 +102,16 @@ def backward_flops(B, H, N, d, causal):
 
 def backward_bytes(B, H, N, d):
     # read Q, K, V, O, dO (bf16) and L; write dQ, dK, dV (bf16)
-    return B * H * N * d * 2 * 8 + B * H * N * 4
+    return traffic.backward_bytes(B, H, N, N, d)
 
 
 def decode_kv_bytes(B, H, Nk, d):
-    return 2 * B * H * Nk * d * 2
+    return traffic.decode_kv_bytes(B, H, Nk, d)
 
 
 def decode_bytes(B, H, Nk, d):
     # K and V once, q in, O out (bf16), L out (fp32)
-    return decode_kv_bytes(B, H, Nk, d) + 2 * B * H * d * 2 + B * H * 4
+    return traffic.decode_bytes(B, H, Nk, d)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -699,7 +703,7 @@ def run_fp8(args):
                      "traffic": recorded_traffic("fp8" if d == 128 else "fp8_64")
                      if (B, H, N) == (1, 32, 8192) and args.window < 0 else None,
                      "traffic_kernel": "prefill_fp8_kernel alone (ncu)",
-                     "algorithmic_bytes": B * H * N * d * 3 + B * H * N * d * 2 + B * H * N * 4},
+                     "algorithmic_bytes": traffic.fp8_forward_bytes(B, H, N, N, d)},
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler is not None else None,
     }
