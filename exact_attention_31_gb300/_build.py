@@ -6,7 +6,9 @@ exports the C ABI declared in include/fattn.h.
 
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -17,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
+STAMP = os.path.join(BUILD, "libfattn.stamp")
 
 SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "prefill_fp8_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu",
            "host_staging.cu"]
@@ -41,15 +44,30 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def source_digest(extra_flags=None) -> str:
+    """Hash of everything the library is built from: the sources, the headers, this file, the flags,
+    the compiler's path and the host architecture (a library built on another machine never
+    matches)."""
+    h = hashlib.sha256()
+    for f in _inputs():
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS + list(extra_flags or [])).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+def up_to_date(extra_flags=None) -> bool:
+    """True when libfattn.so exists and was built here from exactly the current sources."""
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    with open(STAMP) as f:
+        return f.read().strip() == source_digest(extra_flags)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
+    if not force and up_to_date(extra_flags):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -76,6 +94,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(source_digest(extra_flags) + "\n")
     return LIB
 
 

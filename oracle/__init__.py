@@ -19,7 +19,9 @@ Pages cited by the functions below:
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -28,6 +30,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attention_oracle.cpp")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_STAMP = os.path.join(_HERE, "liboracle.stamp")
 _lock = threading.Lock()
 _lib = None
 
@@ -35,15 +38,31 @@ _D = ctypes.POINTER(ctypes.c_double)
 _I64 = ctypes.POINTER(ctypes.c_int64)
 
 
+def _digest(cmd) -> str:
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(cmd).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile ``attention_oracle.cpp`` into ``liboracle.so`` next to it (g++, -O2, no FMA)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
+    """Compile ``attention_oracle.cpp`` into ``liboracle.so`` next to it (g++, -O2, no FMA).  The
+    library is rebuilt whenever the source, the flags or the host architecture differ from those it
+    was built with (recorded in a stamp file beside it)."""
     cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
-           "-pthread", _SRC, "-o", tmp]
-    subprocess.run(cmd, check=True)
+           "-pthread", _SRC, "-o"]
+    digest = _digest(cmd)
+    if not force and os.path.exists(_LIB) and os.path.exists(_STAMP):
+        with open(_STAMP) as f:
+            if f.read().strip() == digest:
+                return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.run(cmd + [tmp], check=True)
     os.replace(tmp, _LIB)
+    with open(_STAMP, "w") as f:
+        f.write(digest + "\n")
     return _LIB
 
 
