@@ -91,16 +91,20 @@ def test_decode_guard_bands_and_workspace_reuse(fa):
     compare(o, None, o_ref, lse_ref, what="decode guard")
 
 
-def test_workload_decode_b32h32_nk16384_d128_sampled(fa):
+@pytest.mark.parametrize("num_splits", [0, 256], ids=["default_splits", "one_state_per_64key_block"])
+def test_workload_decode_b32h32_nk16384_d128(fa, num_splits):
+    # every (b, h) of the B32 H32 Nk16384 d128 decode, element by element against the oracle, with the
+    # default split count and with one partial state per 64-key block; the cache is moved to the host
+    # one batch entry (32 heads, 2 x 128 MiB) at a time
     from exact_attention_31_gb300.workloads import WORKLOADS, make_workload
     w = WORKLOADS["decode_b32h32_nk16384_d128"]
     q, k, v, _ = make_workload(w, "cuda")
-    o, lse = fa.fattn_decode(q, k, v, scale=w.scale)  # one partial state per 64-key block
+    o, lse = fa.fattn_decode(q, k, v, scale=w.scale, num_splits=num_splits)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(5)
-    pairs = [(0, 0), (w.B - 1, w.H - 1)] + [tuple(x) for x in rng.integers(0, [w.B, w.H], size=(14, 2))]
-    for b, h in pairs:
-        o_ref, lse_ref = oracle.attention(to64(q[b:b + 1, h:h + 1]), to64(k[b:b + 1, h:h + 1]),
-                                          to64(v[b:b + 1, h:h + 1]), causal=False, scale=w.scale)
-        compare(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], o_ref, lse_ref, what=f"{w.name} b{b} h{h}")
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    err_sum = 0.0
+    for b in range(w.B):
+        o_ref, lse_ref = oracle.attention(to64(q[b:b + 1]), to64(k[b:b + 1]), to64(v[b:b + 1]), causal=False,
+                                          scale=w.scale)
+        s = compare(o[b:b + 1], lse[b:b + 1], o_ref, lse_ref, what=f"{w.name} b{b}")
+        err_sum += s["o_mean"]
+    assert err_sum / w.B <= 1e-3

@@ -1,7 +1,6 @@
 """GPU parity of fattn_fwd (the tcgen05 prefill kernel) against the fp64 oracle.
 
-Small and mid sizes are compared element by element over every output; the full-size workloads
-are compared on sampled rows that the oracle computes one by one.  All inputs come from the
+Every output is compared element by element, the full-size workloads included.  All inputs come from the
 seeded generator in exact_attention_31_gb300.workloads.
 """
 
@@ -11,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity_utils import compare, oracle_full, oracle_rows, sample_rows, to64
+from parity_utils import compare, oracle_full, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -128,29 +127,31 @@ def test_workload_b1h8_n1024_d64_causal(fa):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_workload_b4h16_n2048_d128_boosted_rows(fa, causal):
+    # every output of the B4 H16 N2048 d128 workload (1 % of the query rows of each head x8),
+    # element by element against the oracle
     from exact_attention_31_gb300.workloads import WORKLOADS, make_workload
     w = WORKLOADS["prefill_b4h16_n2048_d128"]
     q, k, v, boosted = make_workload(w, "cuda")
     o, lse = fa.fattn_fwd(q, k, v, causal=causal, scale=w.scale)
     torch.cuda.synchronize()
-    rows = sample_rows(w.B, w.H, w.Nq, n_heads=6, per_head=48, seed=3 + causal,
-                       extra_per_head=lambda bh: boosted[bh].tolist())
-    o_ref, lse_ref = oracle_rows(q, k, v, rows, causal, w.scale)
-    compare(o.reshape(-1, w.d)[torch.as_tensor(rows, device="cuda")],
-            lse.reshape(-1)[torch.as_tensor(rows, device="cuda")], o_ref, lse_ref, what=w.name)
+    o_ref, lse_ref = oracle_full(q, k, v, causal, w.scale)
+    s = compare(o, lse, o_ref, lse_ref, what=w.name + (" causal" if causal else ""))
+    # the boosted rows on their own (their peaked weights carry the largest errors)
+    rows = np.concatenate([bh * w.Nq + boosted[bh].numpy() for bh in range(w.B * w.H)])
+    ob = to64(o).reshape(-1, w.d)[rows]
+    eb = np.abs(ob - o_ref.reshape(-1, w.d)[rows])
+    assert eb.max() <= 2e-2, (eb.max(), s)
+    assert np.abs(to64(lse).reshape(-1)[rows] - lse_ref.reshape(-1)[rows]).max() <= 1e-3
 
 
-def test_workload_b1h32_n8192_d64_causal_sampled(fa):
+def test_workload_b1h32_n8192_d64_causal(fa):
+    # every output of the B1 H32 N8192 d64 causal workload, element by element against the oracle
     from exact_attention_31_gb300.workloads import WORKLOADS, make_workload
     w = WORKLOADS["prefill_b1h32_n8192_d64"]
     q, k, v, _ = make_workload(w, "cuda")
     o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=w.scale)
     torch.cuda.synchronize()
-    rows = sample_rows(w.B, w.H, w.Nq, n_heads=4, per_head=40, seed=4,
-                       extra_per_head=lambda bh: [255, 256, 8191 - 128, 4095, 4096])
-    o_ref, lse_ref = oracle_rows(q, k, v, rows, True, w.scale)
-    idx = torch.as_tensor(rows, device="cuda")
-    compare(o.reshape(-1, w.d)[idx], lse.reshape(-1)[idx], o_ref, lse_ref, what=w.name)
-    # every row of every head: finite, and the first row of each head is exactly its first value
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    o_ref, lse_ref = oracle_full(q, k, v, True, w.scale)
+    compare(o, lse, o_ref, lse_ref, what=w.name)
+    # causal row 0 sees only key 0: its output is exactly v_0
     assert torch.equal(o[:, :, 0], v[:, :, 0])

@@ -54,7 +54,7 @@ def test_rows_with_rising_scores_are_recomputed_exactly(fa, d, causal):
     o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), causal=causal, scale=scale)
     err = np.abs(to64(o) - o_ref)
     assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (err.max(), err.mean())
-    assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS * max(1.0, np.abs(lse_ref).max() / 64)
+    assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS
 
 
 def test_ordinary_inputs_take_the_fast_path(fa):
@@ -129,4 +129,4 @@ def test_windowed_rows_with_rising_scores(fa, d):
     o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), window=band, scale=scale)
     err = np.abs(to64(o) - o_ref)
     assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (err.max(), err.mean())
-    assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS * max(1.0, np.abs(lse_ref).max() / 64)
+    assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS

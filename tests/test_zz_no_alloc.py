@@ -5,7 +5,8 @@ cudaMalloc (a plugin inside a framework that owns every allocation, or a latency
 cannot afford an allocation's device synchronisation).  For them the library keeps the decode's
 partial states in a fixed array compiled into the library.  These tests call that entry point
 through the C ABI with raw device pointers and check it against fattn_decode, which uses a
-caller-owned workspace, on consecutive calls with different shapes and inputs.
+caller-owned workspace, on consecutive calls with different shapes and inputs, and against the fp64
+oracle on a shape whose split count has to shrink to fit the array.
 This file is collected last on purpose.
 """
 
@@ -42,7 +43,8 @@ def test_static_workspace_decode_matches_workspace_decode():
     from exact_attention_31_gb300.workloads import make_qkv
     L = fa.lib()
     cases = [
-        # B, H, Nk, d, num_splits: the first needs fewer splits than one per 64-key block to fit
+        # B, H, Nk, d, num_splits.  The first fits the array at its default split count (32 splits of
+        # 512 keys: 4.1 MiB of partial states); the last two are given split counts.
         (8, 32, 16384, 128, 0),
         (3, 5, 777, 64, 0),
         (2, 4, 3000, 128, 7),
@@ -58,9 +60,8 @@ def test_static_workspace_decode_matches_workspace_decode():
         torch.cuda.synchronize()
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
         _close(o, lse, o_ref, l_ref)
-        if S:
-            # same split count, same kernels: the results are identical
-            assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+        # same split count, same kernels: the results are identical
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
         # the same call again on the same inputs gives the same bytes (the array's leftovers from
         # the previous call do not leak into the result)
         o2 = torch.empty_like(q)
@@ -68,6 +69,51 @@ def test_static_workspace_decode_matches_workspace_decode():
         assert _raw_static_call(L, q, k, v, o2, lse2, scale, S) == 0
         torch.cuda.synchronize()
         assert torch.equal(o2, o) and torch.equal(lse2, lse)
+
+
+def test_static_workspace_decode_shrinks_the_split_count_to_fit():
+    # The B32 H32 Nk16384 d128 decode: its default 32 splits need 16.6 MiB of partial states, so the
+    # entry point lowers the count until they fit the 8 MiB array (15 splits).  The result must equal
+    # fattn_decode with that count, match the fp64 oracle on sampled heads, and the calls after the
+    # first must not change the device's free memory.
+    import exact_attention_31_gb300 as fa
+    import oracle
+    from exact_attention_31_gb300.workloads import WORKLOADS, make_workload
+    L = fa.lib()
+    w = WORKLOADS["decode_b32h32_nk16384_d128"]
+    q, k, v, _ = make_workload(w, "cuda")
+    assert fa.fattn_decode_workspace_size(w.B, w.H, w.Nk, w.d, 0) > STATIC_BYTES
+    fitted = None
+    for S in range(fa.fattn_decode_num_splits(w.B, w.H, w.Nk, 0), 0, -1):
+        if fa.fattn_decode_workspace_size(w.B, w.H, w.Nk, w.d, S) <= STATIC_BYTES:
+            fitted = S
+            break
+    assert fitted == 15
+    outs = [(torch.full_like(q, float("nan")), torch.full((w.B, w.H, 1), float("nan"), device="cuda"))
+            for _ in range(3)]
+    assert _raw_static_call(L, q, k, v, outs[0][0], outs[0][1], w.scale, 0) == 0
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for o, lse in outs[1:]:
+        assert _raw_static_call(L, q, k, v, o, lse, w.scale, 0) == 0
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+    o_ref, l_ref = fa.fattn_decode(q, k, v, scale=w.scale, num_splits=fitted)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], o_ref) and torch.equal(outs[0][1], l_ref)
+    rng = np.random.default_rng(7)
+    pairs = [(0, 0), (w.B - 1, w.H - 1)] + [tuple(x) for x in rng.integers(0, [w.B, w.H], size=(14, 2))]
+    o, lse = outs[0]
+    for b, h in pairs:
+        to64 = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
+        o_x, l_x = oracle.attention(to64(q[b:b + 1, h:h + 1]), to64(k[b:b + 1, h:h + 1]),
+                                    to64(v[b:b + 1, h:h + 1]), causal=False, scale=w.scale)
+        err = np.abs(to64(o[b, h]) - o_x[0, 0])
+        assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (b, h, err.max())
+        assert abs(float(lse[b, h, 0]) - l_x[0, 0, 0]) <= LSE_MAX_ABS, (b, h)
 
 
 def test_static_workspace_decode_rejects_sizes_beyond_the_array():
