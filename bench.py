@@ -505,6 +505,8 @@ def run_ours(args):
         line["roofline"] = rd
     if args.configs and do_prefill and window is None and rank == 0:
         line["configs_measured"] = measure_configs(fa, dev, stream, peaks)
+    if args.rising and do_prefill and window is None and rank == 0:
+        line["prefill_rising_scores"] = measure_rising_scores(fa, dev, stream, P, pre_avg, peaks)
     if args.cpu_budget > 0:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if e2e is not None:
@@ -765,6 +767,43 @@ def measure_configs(fa, dev, stream, peaks, iters=50):
     return out
 
 
+def measure_rising_scores(fa, dev, stream, P, normal_ms, peaks, iters=10):
+    """The benchmark prefill's shape on inputs whose scores rise by about 150 log2-units after the
+    first 128 keys (every key after the first tile is a large one), so that every query tile but
+    each head's first fails the fast path's range check and is computed again with a running max:
+    the cost of the redo phase at its worst.  Timed like the benchmark prefill (L2 flushed before
+    each launch, CUDA events per launch, mean of `iters`), outside the benchmark's timed region."""
+    import torch
+    from exact_attention_31_gb300.workloads import make_rising_scores
+    B, H, N, d = P["B"], P["H"], P["N"], P["d"]
+    q, k, v = make_rising_scores(B, H, N, N, d, 0xFA77E000 + 7, dev, large_from=128)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale = 1 / math.sqrt(d)
+    before = fa.fattn_fwd_recomputed_rows()
+    fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, stream=stream)
+    torch.cuda.synchronize(dev)
+    rows = fa.fattn_fwd_recomputed_rows() - before
+    for _ in range(2):
+        fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout on the rising-score inputs")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / iters
+    tf = prefill_flops(B, H, N, d, True) / (ms * 1e-3) / 1e12
+    return {"workload": f"prefill_b{B}h{H}_n{N}_d{d} causal, scores rising ~150 log2-units after key 127",
+            "rows_failing_range_check": rows, "rows_total": B * H * N, "ms": round(ms, 4),
+            "tflops": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4),
+            "time_vs_normal_inputs": round(ms / normal_ms, 3)}
+
+
 def run_e2e(fa, dev, stream, args, q, k, v, dq, dk, dv, scale_p, scale_d):
     """The same calls fed from pinned host buffers, copies included in the timing."""
     import torch
@@ -888,6 +927,8 @@ def main(argv=None):
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the smaller prefill configurations (configs_measured)")
+    ap.add_argument("--no-rising", dest="rising", action="store_false",
+                    help="skip the prefill on rising-score inputs (prefill_rising_scores)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -461,7 +461,8 @@ def fattn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float,
 
 
 def fattn_fwd_recomputed_rows() -> int:
-    """Rows the forward recomputed on its exact per-row path on the current device so far (waits
+    """Rows of the forward that failed the fast path's range check (their query tiles computed again
+    with a running max) on the current device so far (waits
     for the device)."""
     out = ctypes.c_ulonglong(0)
     st = lib().fattn_fwd_recomputed_rows(ctypes.byref(out))

@@ -19,7 +19,8 @@ namespace {
 
 // Status word the kernels raise bits in (bounded waits that gave up).  One copy per device.
 __device__ unsigned int g_device_status;
-// Rows of fattn_fwd that the prefill kernel recomputed on its exact per-row path (cumulative).
+// Rows of fattn_fwd that failed the prefill kernel's range check, whose tiles it computed again
+// with a running max (cumulative).
 __device__ unsigned long long g_recomputed_rows;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

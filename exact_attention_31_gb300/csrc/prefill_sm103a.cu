@@ -41,13 +41,21 @@
 // every later step.  What it gives up is a bound on the weights, so each row is checked when its
 // unit ends: with the reference in place its weight sum l is at least 1 (the first max has weight
 // 1), and the row is accepted when l <= 2^64 and every output is finite.  A row that fails (its
-// scores rose by more than about 64 / c over those of its first tile) is recomputed by its own
-// thread in fp32 with an exact max and plain loads, and counted in a device counter.  One row sum
+// scores rose by more than about 64 / c over those of its first tile) marks its 128-row query tile
+// in a per-CTA bitmask and is counted in a device counter.  When the CTA has worked through its
+// units, every role meets at one barrier and the marked tiles are computed again on the tensor
+// cores, as units of their own through the same pipeline, by a softmax that carries the running
+// max and multiplies l and O (in tensor memory) by exp2(m_old - m_new) whenever the max rises, as
+// the pages' correction factor does (the redo phase).  The redo phase's code lives in functions that
+// are not inlined: with it inlined the compiler lays out the main loop differently, and the main
+// loop is the time that matters.  One row sum
 // l of the fp32 weights gives both O / l and L = m + log(l); P V sees the weights rounded to bf16,
 // so O carries a relative bias of at most 2^-9 (one rounding of the dominant weight) on rows with
 // one dominant key.  The per-row arithmetic uses packed fp32x2 FMA/add and three-input max with
 // several independent accumulators, so one thread's row is not a single long dependency chain.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 #include <math.h>
 
 #include "fattn_internal.h"
@@ -64,6 +72,9 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;   // tile 0 (d = 64) or both tiles (d = 128); TMEM owner
 constexpr int kMmaWarp1 = 10; // tile 1 (d = 64)
 constexpr float kWeightSumMax = 0x1p64f;  // a row whose weight sum exceeds this is recomputed
+constexpr float kRescaleLog2 = 0.f;        // redo phase: the running max moves when it rises by more
+constexpr int kRedoWords = 256;            // bitmask of marked query tiles, 2 bits per unit of a CTA
+constexpr int kMaxUnitsPerCta = kRedoWords * 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtomBytes = kBlockM * 128;  // one 128-row x 128-byte swizzled chunk
 
@@ -92,7 +103,8 @@ struct Cfg {
   static constexpr int kNumBars = 18 + 2 * kSlots;
   static constexpr int kMmaWarps = kSepP ? 2 : 1;   // commits that release a K/V slot
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  static constexpr uint32_t kRedoOff = kMiscOff + 16;  // kRedoWords words: tiles to compute again
+  static constexpr uint32_t kSmemBytes = kRedoOff + kRedoWords * 4 + 1024;  // + slack to align the base
   // tensor-memory columns
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
@@ -100,18 +112,16 @@ struct Cfg {
 };
 
 struct Args {
-  const __nv_bfloat16* q;  // [BH, Nq, D], for rows that are recomputed
-  const __nv_bfloat16* k;  // [BH, Nk, D]
-  const __nv_bfloat16* v;  // [BH, Nk, D]
   __nv_bfloat16* o;
   float* lse;
   int BH, Nq, Nk;
   int wl, wr, off;     // mask band: key j visible to row i iff i+off-wl <= j <= i+off+wr (-1 = unbounded)
   int units_per_head;  // ceil(Nq / 256)
-  int total_units;     // BH * units_per_head
+  int unit_base;       // this launch works on units [unit_base, unit_end) of the BH * units_per_head
+  int unit_end;
   float c_log2;        // scale * log2(e)
   unsigned int* status;
-  unsigned long long* recomputed;  // rows recomputed by recompute_row (diagnostic counter)
+  unsigned long long* recomputed;  // rows that failed the range check (diagnostic counter)
   unsigned long long timeout_ns;
   int drop_kv_block;  // failure-detection testing only; -1 = off
 };
@@ -157,14 +167,33 @@ struct Unit {
 // walked backwards so that each CTA's total is closer to the others'.  Returns false past the end.
 __device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  if (idx >= a.total_units) return false;
+  const long long idx = a.unit_base + static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (idx >= a.unit_end) return false;
   const int i = static_cast<int>(idx);
   u.bh = i % a.BH;
   u.row0 = (a.units_per_head - 1 - i / a.BH) * kTiles * kBlockM;
   key_tiles(u.row0, a, u.jb[0], u.je[0]);
   key_tiles(u.row0 + kBlockM, a, u.jb[1], u.je[1]);
   return true;
+}
+
+// Unit k of the CTA again, for the redo phase: only the query tiles marked in `redo` (2 bits per
+// unit; the others emptied).  False when neither is marked.
+__device__ __forceinline__ bool redo_unit(int k, const uint32_t* redo, Unit& u) {
+  const uint32_t bits = (redo[k >> 4] >> ((k & 15) * 2)) & 3u;
+  if (!(bits & 1u)) u.jb[0] = u.je[0] = 0;
+  if (!(bits & 2u)) u.jb[1] = u.je[1] = 0;
+  return bits != 0u;
+}
+
+// Every thread of the CTA calls this once, after its role's main phase: by then every role has issued,
+// and the softmax groups have finished, all of the main phase's work (or some wait gave up and set
+// the abort word), and the marks are visible to every thread.  True when the redo phase runs: some
+// tile was marked (the word after the abort word, set by mark_row) and no wait gave up.
+__device__ __noinline__ bool redo_begin(bool ok, volatile uint32_t* abort_flag) {
+  __syncwarp();
+  named_bar_sync(1, kThreads);
+  return abort_flag[1] != 0u && ok && abort_flag[0] == 0u;
 }
 
 __device__ __forceinline__ void wait_dep(uint32_t (&r)[32]) {
@@ -232,55 +261,32 @@ __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) 
       : "f"(b0), "f"(b1));
 }
 
-// ------------------------------------------------------------------------------------------------
-// One row recomputed by its own thread: O = softmax(scale * q K^T) V over the visible keys
-// [kb, ke] and L, in fp32 from the bf16 inputs with an exact max.  Two passes give the max and the
-// weight sum, then one pass per 32 output columns accumulates P V (each pass recomputes the
-// scores, so only 32 accumulators are live).  Plain loads, O(Nk d) work per row: it serves only
-// the rows the fast path rejected.
-// ------------------------------------------------------------------------------------------------
+// Marks query tile t of the CTA's unit k for the redo phase (bit 2k + t of the shared-memory
+// bitmask) and counts the row.  Out of line, like any rare path here, so that the main loop's code
+// does not change with it.
 template <int D>
-__device__ __noinline__ void recompute_row(const Args& a, int bh, int row, int kb, int ke) {
-  const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(a.q + (static_cast<size_t>(bh) * a.Nq + row) * D);
-  const __nv_bfloat16* kh = a.k + static_cast<size_t>(bh) * a.Nk * D;
-  const __nv_bfloat16* vh = a.v + static_cast<size_t>(bh) * a.Nk * D;
-  const float c = a.c_log2;
-  auto score = [&](int j) {  // q . k_j * c
-    const __nv_bfloat162* kr = reinterpret_cast<const __nv_bfloat162*>(kh + static_cast<size_t>(j) * D);
-    float s0 = 0.f, s1 = 0.f;
-    for (int e = 0; e < D / 2; ++e) {
-      const float2 x = __bfloat1622float2(q[e]), y = __bfloat1622float2(kr[e]);
-      s0 = fmaf(x.x, y.x, s0);
-      s1 = fmaf(x.y, y.y, s1);
-    }
-    return (s0 + s1) * c;
-  };
-  float m = -INFINITY;
-  for (int j = kb; j <= ke; ++j) m = fmaxf(m, score(j));
-  float l = 0.f;
-  for (int j = kb; j <= ke; ++j) l += exp2f(score(j) - m);
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + row) * D;
-  for (int d0 = 0; d0 < D; d0 += 32) {
-    float acc[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-    for (int j = kb; j <= ke; ++j) {
-      const float p = exp2f(score(j) - m);
-      const __nv_bfloat162* vr = reinterpret_cast<const __nv_bfloat162*>(vh + static_cast<size_t>(j) * D + d0);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float2 y = __bfloat1622float2(vr[e]);
-        acc[2 * e] = fmaf(p, y.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(p, y.y, acc[2 * e + 1]);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) orow[d0 + e] = __float2bfloat16_rn(acc[e] * inv_l);
-  }
-  if (a.lse != nullptr)
-    a.lse[static_cast<size_t>(bh) * a.Nq + row] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+__device__ __noinline__ void mark_row(const Args& a, uint32_t sbar, int k, int t) {
+  const uint32_t word = sbar - Cfg<D>::kBarOff + Cfg<D>::kRedoOff + 4u * static_cast<uint32_t>(k >> 4);
+  asm volatile("red.shared.or.b32 [%0], %1;" ::"r"(word), "r"(1u << ((k & 15) * 2 + t)) : "memory");
+  const uint32_t any = sbar - Cfg<D>::kBarOff + Cfg<D>::kMiscOff + 8u;  // "some tile is marked"
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(any), "r"(1u) : "memory");
   atomicAdd(a.recomputed, 1ull);
+}
+
+// Max of a row's 128 scores in eight independent chains of three-input maxes: fewer live temporaries
+// than the tree below (the redo phase takes it at every step, with all 128 scores live).
+__device__ __forceinline__ float max128_chains(const uint32_t (&s)[4][32]) {
+  float mx8[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[0][2 * k]), __uint_as_float(s[0][2 * k + 1]));
+#pragma unroll
+  for (int e = 16; e < 128; e += 16) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mx8[k] = max3f(mx8[k], __uint_as_float(s[(e + 2 * k) >> 5][(e + 2 * k) & 31]),
+                     __uint_as_float(s[(e + 2 * k + 1) >> 5][(e + 2 * k + 1) & 31]));
+  }
+  return fmaxf(max3f(mx8[0], mx8[1], mx8[2]), fmaxf(max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
 }
 
 // Max of a row's 128 scores as a balanced tree of three-input maxes: 66 instructions, five deep (the
@@ -306,8 +312,18 @@ __device__ __forceinline__ float max128_tree(const uint32_t (&s)[4][32]) {
 // ------------------------------------------------------------------------------------------------
 // g counts tile t's steps over all units of this CTA (the phase of S_full, P_full, PV_done);
 // done counts its non-empty units (the phase of O_full and O_free).
-template <int D>
-__device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
+//
+// kRunning = false (the main phase): the exponent reference is fixed at the max of the row's first
+// tile with a visible key; a tile with a row that fails the range check at the end is marked in
+// `redo` (bit 2k + t, k the CTA's unit index) for the redo phase.
+// kRunning = true (the redo phase): every step takes the tile's row max, and when it exceeds the
+// reference by more than kRescaleLog2 the reference moves up to it and l and O are multiplied by
+// exp2(m_old - m_new) ("Flash Attention: The Hidden Gem", The Correction Factor), so every weight
+// stays below 2^kRescaleLog2.  With kRescaleLog2 = 0 the row's largest weight is exactly 1, which
+// bf16 holds exactly: the rows that land here are the ones whose large weights come late, and a
+// rounded dominant weight would bias their O by up to 2^-9 of its size.
+template <int D, bool kRunning>
+__device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
                                              uint32_t sbar, const Args& a, const Abort& ab, int& g, int& done) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -324,7 +340,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   const uint32_t tP = tmem + lane_field + C::col_p(t);
   const float c = a.c_log2;
 
-  float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score (set once per unit)
+  float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
   float l = 0.f;            // sum of the fp32 weights: O = O / l, L = m + log(l)
   bool ok = true;
   for (int step = 0; step < n_tiles; ++step, ++g) {
@@ -375,11 +391,23 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
             if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
       }
     }
-    // The reference is the max of the row's first key tile that holds a visible key; later tiles
-    // leave it in place.
-    if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
-      const float mx = max128_tree(s);
-      if (m_ref == -INFINITY) m_ref = mx * c;
+    float corr = 1.f;  // redo phase: factor for l and O when the reference moved in this step
+    bool moved = false;
+    if constexpr (kRunning) {
+      const float m_new = fmaxf(m_ref, max128_chains(s) * c);
+      if (m_new > m_ref + kRescaleLog2) {
+        corr = ex2_approx(m_ref - m_new);  // 0 while no key has been seen
+        m_ref = m_new;
+        l *= corr;
+        moved = true;
+      }
+    } else {
+      // The reference is the max of the row's first key tile that holds a visible key; later tiles
+      // leave it in place.
+      if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+        const float mx = max128_tree(s);
+        if (m_ref == -INFINITY) m_ref = mx * c;
+      }
     }
     const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
@@ -412,6 +440,26 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     if (!pv_ok) {
       ok = false;
       break;
+    }
+    if constexpr (kRunning) {
+      // O_t was last written by P_t(j-1) V_{j-1}, which has completed: with a separate P its
+      // completion was awaited before the P store above; with P over S, S_t(j) was issued after it.
+      if (step > 0 && __any_sync(0xffffffffu, moved)) {
+#pragma unroll
+        for (int h = 0; h < D / 32; ++h) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + 32 * h, o);
+          wait_dep(o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float y0, y1;
+            ffma2_bc(y0, y1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), corr, 0.f);
+            o[i] = __float_as_uint(y0);
+            o[i + 1] = __float_as_uint(y1);
+          }
+          tmem_st_32x32b_x32(tO + 32 * h, o);
+        }
+      }
     }
     tmem_wait_st();
     tc_fence_before();
@@ -449,12 +497,14 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float y0 = __uint_as_float(o[2 * i]) * inv_l, y1 = __uint_as_float(o[2 * i + 1]) * inv_l;
-      if (i & 1) {
-        fin2 = fmaf(y0, 0x1p-8f, fin2);
-        fin3 = fmaf(y1, 0x1p-8f, fin3);
-      } else {
-        fin = fmaf(y0, 0x1p-8f, fin);
-        fin1 = fmaf(y1, 0x1p-8f, fin1);
+      if constexpr (!kRunning) {
+        if (i & 1) {
+          fin2 = fmaf(y0, 0x1p-8f, fin2);
+          fin3 = fmaf(y1, 0x1p-8f, fin3);
+        } else {
+          fin = fmaf(y0, 0x1p-8f, fin);
+          fin1 = fmaf(y1, 0x1p-8f, fin1);
+        }
       }
       pk[i] = pack_bf16x2(y0, y1);
     }
@@ -473,102 +523,174 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
   if (store && a.lse != nullptr) {
     a.lse[static_cast<size_t>(bh) * a.Nq + q_row] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
-  // A row with a visible key has l >= 1 (the reference's own weight); it is accepted when l stayed
-  // within kWeightSumMax (no weight overflowed or approached the fp32 range) and its outputs are
-  // finite.  Otherwise its thread recomputes it.
-  const int k_lo = max(lo, 0);
-  const bool accepted = l >= 0.5f && l <= kWeightSumMax && fabsf(fin) <= 3.4028234663852886e38f;
-  if (store && k_lo <= hi && !accepted) recompute_row<D>(a, bh, q_row, k_lo, hi);
+  if constexpr (!kRunning) {
+    // A row with a visible key has l >= 1 (the reference's own weight); it is accepted when l stayed
+    // within kWeightSumMax (no weight overflowed or approached the fp32 range) and its outputs are
+    // finite.  Otherwise the tile is computed again in the redo phase.
+    const int k_lo = max(lo, 0);
+    const bool accepted = l >= 0.5f && l <= kWeightSumMax && fabsf(fin) <= 3.4028234663852886e38f;
+    if (store && k_lo <= hi && !accepted) mark_row<D>(a, sbar, k, t);
+  }
   __syncwarp();
   return true;
 }
 
+// The redo phase of softmax group t (a function of its own, so that its code does not change the
+// main phase's): the marked tiles again with a running max, barrier phases continued from g, done.
 template <int D>
-__device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab) {
+__device__ __noinline__ bool softmax_unit_running(int t, int k, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
+                                                  uint32_t sbar, const Args& a, const Abort& ab, int& g, int& done) {
+  return softmax_unit<D, true>(t, k, jb, n_tiles, row0, bh, tmem, sbar, a, ab, g, done);
+}
+
+template <int D>
+__device__ __noinline__ void softmax_tail(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab, int g,
+                                          int done, uint32_t* redo, bool ok) {
+  if (!redo_begin(ok, ab.flag)) return;
+  Unit u;
+  for (int k = 0; cta_unit(k, a, u); ++k) {
+    if (!redo_unit(k, redo, u) || u.je[t] == u.jb[t]) continue;
+    ab.renew(a.timeout_ns);
+    if (!softmax_unit_running<D>(t, k, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done))
+      return;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab,
+                                             uint32_t* redo) {
   int g = 0, done = 0;
+  bool ok = true;
   Unit u;
   for (int k = 0; cta_unit(k, a, u); ++k) {
     ab.renew(a.timeout_ns);
-    if (!softmax_unit<D>(t, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done)) return;
+    if (!softmax_unit<D, false>(t, k, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done)) {
+      ok = false;
+      break;
+    }
   }
+  softmax_tail<D>(t, tmem, sbar, a, ab, g, done, redo, ok);
 }
 
 // ------------------------------------------------------------------------------------------------
 // TMA producer (one thread)
 // ------------------------------------------------------------------------------------------------
+struct ProducerState {
+  int ring = 0;            // K/V ring index of the unit's first key tile (2 per key tile, over all units)
+  int qloads[2] = {0, 0};  // Q_t loads issued so far (the phase of Q_full / Q_free)
+  int issued = 0;          // ring index one past the last K/V load issued
+  int dropped = -1;        // ring index of the load skipped for failure-detection testing
+};
+
+// One unit's loads: Q of its non-empty tiles, then K_j and V_j for the union of the two tiles' ranges
+// (ring index ring + 2 (j - J0) + w).  False when a wait gave up.
 template <int D>
-__device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk,
-                                              const CUtensorMap* tv, uint32_t sbase, const Args& a, Abort ab) {
+__device__ __forceinline__ bool producer_unit(const Unit& u, const CUtensorMap* tq, const CUtensorMap* tk,
+                                              const CUtensorMap* tv, uint32_t sbase, const Args& a,
+                                              const Abort& ab, ProducerState& ps) {
   using C = Cfg<D>;
   const uint32_t sbar = sbase + C::kBarOff;
-  tma_prefetch_desc(tq);
-  tma_prefetch_desc(tk);
-  tma_prefetch_desc(tv);
-  int ring = 0;           // K/V ring index of the unit's first key tile (2 per key tile, over all units)
-  int qloads[2] = {0, 0}; // Q_t loads issued so far (the phase of Q_full / Q_free)
-  int issued = 0;         // ring index one past the last K/V load issued
-  int dropped = -1;       // ring index of the load skipped for failure-detection testing
-  bool ok = true;
-  Unit u;
-  for (int k = 0; ok && cta_unit(k, a, u); ++k) {
-    ab.renew(a.timeout_ns);
 #pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-      if (u.je[t] == u.jb[t]) continue;
-      // Q_t's buffer is free once the previous unit's last S_t has read it.
-      if (qloads[t] > 0 && !thread_wait(sbar + 8 * (C::kQFree + t), (qloads[t] - 1) & 1, ab)) {
-        ok = false;
-        break;
+  for (int t = 0; t < kTiles; ++t) {
+    if (u.je[t] == u.jb[t]) continue;
+    // Q_t's buffer is free once the previous unit's last S_t has read it.
+    if (ps.qloads[t] > 0 && !thread_wait(sbar + 8 * (C::kQFree + t), (ps.qloads[t] - 1) & 1, ab)) return false;
+    const uint32_t bar = sbar + 8 * (C::kQFull + t);
+    mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+    for (int ch = 0; ch < C::kChunks; ++ch)
+      tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + ch * kAtomBytes, tq, bar, ch * 64, u.row0 + t * kBlockM,
+                  u.bh);
+    ++ps.qloads[t];
+  }
+  const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
+  for (int j = J0; j < J1; ++j) {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int idx = ps.ring + 2 * (j - J0) + w;
+      const int slot = idx % C::kSlots;
+      const int round = idx / C::kSlots;
+      if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) return false;
+      ps.issued = idx + 1;
+      if (w == 0 && j == a.drop_kv_block) {  // testing only: this tile never arrives
+        ps.dropped = idx;
+        continue;
       }
-      const uint32_t bar = sbar + 8 * (C::kQFull + t);
+      const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
       mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
       for (int ch = 0; ch < C::kChunks; ++ch)
-        tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + ch * kAtomBytes, tq, bar, ch * 64,
-                    u.row0 + t * kBlockM, u.bh);
-      ++qloads[t];
+        tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + ch * kAtomBytes, w ? tv : tk, bar, ch * 64,
+                    j * kBlockN, u.bh);
     }
-    if (!ok) break;
-    // K_j and V_j for the union of the two tiles' ranges; ring index ring + 2 (j - J0) + w
-    const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
-    for (int j = J0; j < J1 && ok; ++j) {
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const int idx = ring + 2 * (j - J0) + w;
-        const int slot = idx % C::kSlots;
-        const int round = idx / C::kSlots;
-        if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) {
-          ok = false;
-          break;
-        }
-        issued = idx + 1;
-        if (w == 0 && j == a.drop_kv_block) {  // testing only: this tile never arrives
-          dropped = idx;
-          continue;
-        }
-        const uint32_t bar = sbar + 8 * (C::kKVFull + slot);
-        mbar_arrive_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-        for (int ch = 0; ch < C::kChunks; ++ch)
-          tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + ch * kAtomBytes, w ? tv : tk, bar,
-                      ch * 64, j * kBlockN, u.bh);
+  }
+  if (J1 > J0) ps.ring += 2 * (J1 - J0);
+  return true;
+}
+
+template <int D>
+__device__ __noinline__ bool producer_unit_redo(const Unit& u, const CUtensorMap* tq, const CUtensorMap* tk,
+                                                const CUtensorMap* tv, uint32_t sbase, const Args& a, const Abort& ab,
+                                                ProducerState& ps) {
+  return producer_unit<D>(u, tq, tk, tv, sbase, a, ab, ps);
+}
+
+// The producer's redo phase and wind-down (whole warp; lane 0 issues).  After a wait gave up, the
+// copies already in flight land before the CTA's shared memory goes away.
+template <int D>
+__device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                           uint32_t sbase, const Args& a, Abort ab, ProducerState ps, bool ok,
+                                           uint32_t* redo) {
+  using C = Cfg<D>;
+  const uint32_t sbar = sbase + C::kBarOff;
+  const bool lead = (threadIdx.x & 31) == 0;
+  if (redo_begin(ok, ab.flag) && lead) {
+    Unit u;
+    for (int k = 0; cta_unit(k, a, u); ++k) {
+      if (!redo_unit(k, redo, u)) continue;
+      ab.renew(a.timeout_ns);
+      if (!producer_unit_redo<D>(u, tq, tk, tv, sbase, a, ab, ps)) {
+        ok = false;
+        break;
       }
     }
-    if (J1 > J0) ring += 2 * (J1 - J0);
   }
-  if (!ok) {
-    // Let the copies already in flight land before the CTA's shared memory goes away.
+  if (lead && !ok) {
     const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
     volatile uint32_t never = 0;
-    for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx) {
-      if (idx == dropped) continue;
+    for (int idx = max(0, ps.issued - C::kSlots); idx < ps.issued; ++idx) {
+      if (idx == ps.dropped) continue;
       const int slot = idx % C::kSlots;
       mbar_wait_bounded(sbar + 8 * (C::kKVFull + slot), (idx / C::kSlots) & 1, &never, until);
     }
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
-      if (qloads[t] > 0) mbar_wait_bounded(sbar + 8 * (C::kQFull + t), (qloads[t] - 1) & 1, &never, until);
+      if (ps.qloads[t] > 0) mbar_wait_bounded(sbar + 8 * (C::kQFull + t), (ps.qloads[t] - 1) & 1, &never, until);
   }
+  __syncwarp();
+}
+
+// Whole warp; lane 0 issues the main phase's loads.
+template <int D>
+__device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                              uint32_t sbase, const Args& a, Abort ab, uint32_t* redo) {
+  ProducerState ps;
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    tma_prefetch_desc(tq);
+    tma_prefetch_desc(tk);
+    tma_prefetch_desc(tv);
+    Unit u;
+    for (int k = 0; cta_unit(k, a, u); ++k) {
+      ab.renew(a.timeout_ns);
+      if (!producer_unit<D>(u, tq, tk, tv, sbase, a, ab, ps)) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  producer_tail<D>(tq, tk, tv, sbase, a, ab, ps, ok, redo);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -734,10 +856,45 @@ __device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D
   return true;
 }
 
+template <int D>
+__device__ __noinline__ bool mma_unit_redo(int tt, const Unit& u, const MmaCtx<D>& m, MmaState& st, const Abort& ab) {
+  using C = Cfg<D>;
+  bool ok = true;
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t)
+    if ((!C::kSepP || t == tt) && u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
+  if (ok) ok = C::kSepP ? mma_unit_tile<D>(tt, u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
+  return ok;
+}
+
+// The MMA warp's redo phase and wind-down: before the CTA winds down, every MMA (and every arrival
+// its commits make on this CTA's barriers) has completed, on the normal path and after a timeout
+// alike.
+template <int D>
+__device__ __noinline__ void mma_tail(int tt, const MmaCtx<D>& m, MmaState st, const Args& a, Abort ab, bool ok,
+                                      uint32_t* redo) {
+  using C = Cfg<D>;
+  if (redo_begin(ok, ab.flag)) {
+    Unit u;
+    for (int k = 0; ok && cta_unit(k, a, u); ++k) {
+      if (!redo_unit(k, redo, u)) continue;
+      ab.renew(a.timeout_ns);
+      ok = mma_unit_redo<D>(tt, u, m, st, ab);
+    }
+  }
+  const int drain = tt ? C::kDrain1 : C::kDrain;
+  m.commit(drain);
+  volatile uint32_t never = 0;
+  const uint64_t until = ok ? ab.deadline : globaltimer_ns() + 50ull * 1000 * 1000;
+  mbar_wait_bounded(m.sbar + 8 * drain, 0, &never, until);
+  __syncwarp();
+}
+
 // Whole warp.  `tt` is the query tile of this warp (d = 64); with d = 128 the one MMA warp (tt = 0)
 // issues both tiles' products.
 template <int D>
-__device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, const Args& a, Abort ab) {
+__device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, const Args& a, Abort ab,
+                                         uint32_t* redo) {
   using C = Cfg<D>;
   MmaCtx<D> m;
   m.init(tmem, sbase);
@@ -751,14 +908,7 @@ __device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, 
       if ((!C::kSepP || t == tt) && u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
     if (ok) ok = C::kSepP ? mma_unit_tile<D>(tt, u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
   }
-  // Before the CTA winds down, every MMA (and every arrival its commits make on this CTA's
-  // barriers) has completed, on the normal path and after a timeout alike.
-  const int drain = tt ? C::kDrain1 : C::kDrain;
-  m.commit(drain);
-  volatile uint32_t never = 0;
-  const uint64_t until = ok ? ab.deadline : globaltimer_ns() + 50ull * 1000 * 1000;
-  mbar_wait_bounded(m.sbar + 8 * drain, 0, &never, until);
-  __syncwarp();
+  mma_tail<D>(tt, m, st, a, ab, ok, redo);
 }
 
 template <int D>
@@ -773,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbar = sbase + C::kBarOff;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  uint32_t* redo = reinterpret_cast<uint32_t*>(smem + C::kRedoOff);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -793,8 +944,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sbar + 8 * (C::kKVEmpty + s), C::kMmaWarps);
     }
     *abort_flag = 0u;
+    abort_flag[1] = 0u;  // "some tile is marked"
     fence_mbarrier_init();
   }
+  for (int w = threadIdx.x; w < kRedoWords; w += kThreads) redo[w] = 0u;
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -805,15 +958,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   Abort ab{abort_flag, a.status, globaltimer_ns() + a.timeout_ns};
 
+  // Each role works through the CTA's units, then meets the others at one barrier (redo_begin) and
+  // computes the marked tiles again.
   if (warp < 8) {
-    softmax_role<D>(warp >> 2, tmem, sbar, a, ab);
+    softmax_role<D>(warp >> 2, tmem, sbar, a, ab, redo);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, sbase, a, ab);
-    __syncwarp();
+    producer_role<D>(&tm_q, &tm_k, &tm_v, sbase, a, ab, redo);
   } else if (warp == kMmaWarp) {
-    mma_role<D>(0, tmem, sbase, a, ab);
+    mma_role<D>(0, tmem, sbase, a, ab, redo);
   } else if (C::kSepP && warp == kMmaWarp1) {
-    mma_role<D>(1, tmem, sbase, a, ab);
+    mma_role<D>(1, tmem, sbase, a, ab, redo);
+  } else {
+    redo_begin(true, abort_flag);  // (d = 128: the spare warp only takes part in the barrier)
   }
 
   tc_fence_before();
@@ -840,9 +996,6 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   Args a;
-  a.q = static_cast<const __nv_bfloat16*>(p.q);
-  a.k = static_cast<const __nv_bfloat16*>(p.k);
-  a.v = static_cast<const __nv_bfloat16*>(p.v);
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.lse = p.lse;
   a.BH = p.B * p.H;
@@ -852,7 +1005,6 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.wr = p.window_right;
   a.off = p.Nk - p.Nq;
   a.units_per_head = (p.Nq + kTiles * kBlockM - 1) / (kTiles * kBlockM);
-  a.total_units = a.units_per_head * a.BH;
   a.c_log2 = p.scale * 1.4426950408889634f;
   a.status = status;
   a.recomputed = p.recomputed;
@@ -867,9 +1019,20 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
     if (dev >= 0 && dev < 64) sm_count[dev] = n;
     else return cudaErrorInvalidDevice;
   }
-  const unsigned int grid = static_cast<unsigned int>(min(a.total_units, sm_count[dev]));
-  prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  // A CTA marks the tiles to compute again in a bitmask of kMaxUnitsPerCta units, so one launch
+  // covers at most grid * kMaxUnitsPerCta units; larger problems take several launches.
+  const long long total = static_cast<long long>(a.units_per_head) * a.BH;
+  const long long grid = std::min<long long>(total, sm_count[dev]);
+  const long long per_launch = grid * kMaxUnitsPerCta;
+  for (long long base = 0; base < total; base += per_launch) {
+    a.unit_base = static_cast<int>(base);
+    a.unit_end = static_cast<int>(std::min(total, base + per_launch));
+    const unsigned int g = static_cast<unsigned int>(std::min<long long>(grid, a.unit_end - a.unit_base));
+    prefill_kernel<D><<<g, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -124,6 +124,32 @@ def make_dout(B: int, H: int, Nq: int, d: int, seed: int, device="cpu"):
     return _randn_bf16((B, H, Nq, d), gen, device, chunk)
 
 
+def make_rising_scores(B: int, H: int, Nq: int, Nk: int, d: int, seed: int, device="cpu", large_from=None):
+    """Inputs whose scores rise sharply after the first keys (late "attention sinks"): every query
+    is 30 u plus N(0, 0.01) noise for one seeded unit vector u; keys [large_from, Nk) are 30 u plus
+    the same noise (scores near 900 before scaling) and the others, like the values, iid N(0, 1)
+    (scores of about 30 N(0, 1)).  large_from defaults to the last 128 keys.  Drawn in fp32 on
+    `device` from one seeded generator and rounded once to bf16.  Returns (q, k, v)."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    large_from = Nk - 128 if large_from is None else int(large_from)
+    u = torch.randn(d, generator=gen, device=device, dtype=torch.float32)
+    u /= u.norm()
+    q = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=device)
+    k = torch.empty((B, H, Nk, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty((B, H, Nk, d), dtype=torch.bfloat16, device=device)
+    for b in range(B):  # one batch entry at a time bounds the fp32 temporaries
+        q[b] = 30 * u + 0.1 * torch.randn((H, Nq, d), generator=gen, device=device)
+        kb = torch.randn((H, Nk, d), generator=gen, device=device)
+        if large_from < Nk:
+            kb[:, max(large_from, 0):] = 30 * u + 0.1 * torch.randn((H, Nk - max(large_from, 0), d), generator=gen,
+                                                                       device=device)
+        k[b] = kb
+        v[b] = torch.randn((H, Nk, d), generator=gen, device=device)
+    return q, k, v
+
+
 def quantize_e4m3(x: torch.Tensor):
     """Per-tensor e4m3 quantisation of a float tensor: scale so that the largest magnitude maps to
     448 (e4m3's largest finite value), round to nearest.  Returns (x_e4m3, descale) with

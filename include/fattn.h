@@ -62,9 +62,11 @@ typedef enum fattn_status {
  * Numerics: each row's exponent reference is the max of its first key tile with a visible key
  * and is not raised afterwards (softmax is unchanged by the choice of reference, The Correction
  * Factor).  A row whose weights then leave a safe range (weight sum above 2^64, i.e. scores more
- * than about 64 log2-units above those of its first tile, or a non-finite output) is recomputed
- * by the kernel on a per-row path in fp32 with an exact max (slower, O(Nk d) per row); the result
- * is within the same tolerance either way.  fattn_fwd_recomputed_rows counts such rows.
+ * than about 64 log2-units above those of its first tile, or a non-finite output) marks its
+ * 128-row query tile, and the kernel computes the marked tiles again on the tensor cores, after
+ * its other work, with the running max and the O rescale of The Correction Factor (at most about
+ * twice the time when every tile is marked); the result is within the same tolerance either way.
+ * fattn_fwd_recomputed_rows counts such rows.
  */
 fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                        int Nq, int Nk, int d, int causal, float scale, void* stream);
@@ -297,9 +299,9 @@ fattn_status fattn_decode_host(const void* q_host, const void* k_host, const voi
 fattn_status fattn_last_error(void* stream);
 
 /*
- * fattn_fwd_recomputed_rows -- the number of rows that fattn_fwd and fattn_fwd_masked recomputed on
- * their exact per-row path on the current device since the library was loaded (a diagnostic; see
- * fattn_fwd, Numerics).  Waits for all work on the current device first.  *out must not be NULL
+ * fattn_fwd_recomputed_rows -- the number of rows of fattn_fwd and fattn_fwd_masked that failed the
+ * fast path's range check on the current device since the library was loaded, and whose query
+ * tiles were therefore computed again with a running max (a diagnostic; see fattn_fwd, Numerics).  Waits for all work on the current device first.  *out must not be NULL
  * (FATTN_ERR_INVALID_ARG); FATTN_ERR_CUDA if the device reported an error.
  */
 fattn_status fattn_fwd_recomputed_rows(unsigned long long* out);

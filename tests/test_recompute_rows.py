@@ -1,8 +1,9 @@
-"""GPU parity of the forward's exact per-row path.
+"""GPU parity of the forward's redo phase.
 
 Each row's exponent reference is the max of its first key tile with a visible key; a row whose later
-scores rise far above it (weight sum above 2^64) is recomputed by the kernel on its per-row path.
-These inputs force that path: every query is 30 u plus small noise for one unit vector u, the keys of
+scores rise far above it (weight sum above 2^64) marks its 128-row query tile, and the kernel computes
+the marked tiles again on the tensor cores with a running max (the correction-factor rescale of O in
+tensor memory) once it has worked through its other units.  These inputs force that path: every query is 30 u plus small noise for one unit vector u, the keys of
 the last 128-key tile are 30 u plus noise (scores near 900, about 160 log2-units after scaling) and
 the other keys are N(0, 1) (scores about 30 N(0, 1)).  Rows that see the last tile must be
 recomputed, the others must not, and every output must match the fp64 oracle.
@@ -66,29 +67,41 @@ def test_ordinary_inputs_take_the_fast_path(fa):
 
 
 def test_backward_from_recomputed_rows(fa):
-    # O and L of recomputed rows feed the backward like those of the exact forward: the backward
-    # run from them matches the same backward run from the oracle's O and L.  (Against the oracle's
-    # gradients these inputs are ill-conditioned: k = 30 u + noise makes dq = sum_j dS_j k_j cancel
-    # its 30 u part, since sum_j dS_j = 0, which magnifies the bf16 rounding of dS.)
+    # O and L of recomputed rows feed the backward like those of the exact forward: the backward run
+    # from the forward's O and L matches the same backward run from the oracle's O and L.  (Both
+    # carry the backward's own error at scores this large, which the comparison cancels.)  The
+    # queries are 80 u plus small noise, the last key tile 8 u plus N(0, 1) noise: scores near 640
+    # against about 208 for the first tile's max, so every row's tile is recomputed.  The gradient
+    # is sensitive to O through D = rowsum(dO o O): a change dD_i moves dq_i by -scale dD_i sum_j
+    # P_ij k_j, about dD_i here since |k| is small, well inside the tolerance.
     from exact_attention_31_gb300.workloads import make_dout
-    B, H, N, d = 1, 1, 384, 64
-    q, k, v = rising_scores(B, H, N, d, 4600)
+    B, H, N, d = 1, 2, 384, 64
+    g = torch.Generator().manual_seed(4600)
+    u = torch.randn(d, generator=g, dtype=torch.float64)
+    u /= u.norm()
+    q = 80 * u + 0.1 * torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    k = torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    k[:, :, N - 128:] = 8 * u + torch.randn(B, H, 128, d, generator=g, dtype=torch.float64)
+    v = torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    q, k, v = (t.to(torch.bfloat16).cuda() for t in (q, k, v))
     do = make_dout(B, H, N, d, 4600, device="cuda")
     scale = 1.0 / math.sqrt(d)
     before = fa.fattn_fwd_recomputed_rows()
     o, lse = fa.fattn_fwd(q, k, v, causal=False, scale=scale)
-    assert fa.fattn_fwd_recomputed_rows() - before == N
+    assert fa.fattn_fwd_recomputed_rows() - before == B * H * N
+    # (the forward's own accuracy on rising scores is checked by the tests above; these inputs are
+    # far more peaked than the contract's N(0, 1) ones)
     o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), causal=False, scale=scale)
     o_x = torch.from_numpy(o_ref).to(torch.bfloat16).cuda()
     lse_x = torch.from_numpy(lse_ref).to(torch.float32).cuda()
     g_fwd = fa.fattn_bwd(q, k, v, o, lse, do, causal=False, scale=scale)
     g_exact = fa.fattn_bwd(q, k, v, o_x, lse_x, do, causal=False, scale=scale)
     torch.cuda.synchronize()
-    # The two O differ by up to one bf16 rounding, which the cancellation above magnifies in dq to a
-    # few bf16 ulps; a wrong L would move every gradient by O(1).
     for name, a_, b_ in zip(("dq", "dk", "dv"), g_fwd, g_exact):
         a64, b64 = to64(a_), to64(b_)
-        assert np.abs(a64 - b64).max() <= 5e-2 * np.abs(b64).max(), name
+        e = np.abs(a64 - b64)
+        assert e.max() <= 1.5e-2 * np.abs(b64).max() and e.mean() <= 5e-3 * np.abs(b64).mean(), \
+            (name, e.max(), np.abs(b64).max(), e.mean(), np.abs(b64).mean())
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -130,3 +143,48 @@ def test_windowed_rows_with_rising_scores(fa, d):
     err = np.abs(to64(o) - o_ref)
     assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (err.max(), err.mean())
     assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS
+
+
+def _check(o, lse, q, k, v, scale, what, **kw):
+    o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale=scale, **kw)
+    err = np.abs(to64(o) - o_ref)
+    assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (what, err.max(), err.mean())
+    assert np.abs(to64(lse) - lse_ref).max() <= LSE_MAX_ABS, what
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_long_rows_are_recomputed_without_timeout(fa, d):
+    # 256 queries against 65536 keys, the last 128 keys large: every row's tile is computed again in
+    # the redo phase over 512 key tiles, on the tensor cores, well inside the bounded waits' limit.
+    from exact_attention_31_gb300.workloads import make_rising_scores
+    B, H, Nq, Nk = 1, 1, 256, 65536
+    q, k, v = make_rising_scores(B, H, Nq, Nk, d, 4800 + d, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        before = fa.fattn_fwd_recomputed_rows()
+        o, lse = fa.fattn_fwd(q, k, v, causal=causal, scale=scale)
+        torch.cuda.synchronize()
+        assert fa.fattn_last_error() == 0
+        # bottom-right causal: row i sees keys up to i + Nk - Nq, so rows 128.. see the large keys
+        assert fa.fattn_fwd_recomputed_rows() - before == (128 if causal else 256)
+        _check(o, lse, q, k, v, scale, f"Nk=65536 d={d} causal={causal}", causal=causal)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_every_tile_recomputed(fa, d):
+    # Every key tile after the first is large, so every query tile of every head but the first is
+    # marked: the redo phase computes almost the whole problem again.
+    from exact_attention_31_gb300.workloads import make_rising_scores
+    B, H, N = 2, 3, 1000
+    q, k, v = make_rising_scores(B, H, N, N, d, 4900 + d, device="cuda", large_from=128)
+    scale = 1.0 / math.sqrt(d)
+    before = fa.fattn_fwd_recomputed_rows()
+    o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    assert fa.fattn_fwd_recomputed_rows() - before == B * H * (N - 128)
+    _check(o, lse, q, k, v, scale, f"every tile d={d}", causal=True)
+    # the same call again gives the same bytes
+    o2, lse2 = fa.fattn_fwd(q, k, v, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
