@@ -36,6 +36,7 @@ _lib = None
 
 _D = ctypes.POINTER(ctypes.c_double)
 _I64 = ctypes.POINTER(ctypes.c_int64)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
 
 
 def _digest(cmd) -> str:
@@ -80,15 +81,15 @@ def _load():
         lib.oracle_online_normalizer.argtypes = [_D, ctypes.c_int64, _D, _D]
         lib.oracle_online_normalizer.restype = None
         lib.oracle_attention.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int64] * 7 + [
-            ctypes.c_double, ctypes.c_int]
+            _U8, ctypes.c_double, ctypes.c_int]
         lib.oracle_attention.restype = ctypes.c_int64
         lib.oracle_attention_rows.argtypes = [_D, _D, _D, _I64, ctypes.c_int64, _D, _D] + [
-            ctypes.c_int64] * 7 + [ctypes.c_double, ctypes.c_int]
+            ctypes.c_int64] * 7 + [_U8, ctypes.c_double, ctypes.c_int]
         lib.oracle_attention_rows.restype = ctypes.c_int64
-        lib.oracle_attention_probs.argtypes = [_D, _D] + [ctypes.c_int64] * 5 + [ctypes.c_double, _D]
+        lib.oracle_attention_probs.argtypes = [_D, _D] + [ctypes.c_int64] * 5 + [_U8, ctypes.c_double, _D]
         lib.oracle_attention_probs.restype = None
         lib.oracle_attention_backward.argtypes = [_D] * 7 + [ctypes.c_int64] * 7 + [
-            ctypes.c_double, ctypes.c_int]
+            _U8, ctypes.c_double, ctypes.c_int]
         lib.oracle_attention_backward.restype = None
         _lib = lib
         return lib
@@ -144,6 +145,15 @@ def band(causal: bool = False, window=None) -> tuple[int, int]:
     return (-1, 0) if causal else (-1, -1)
 
 
+def _mask_u8(mask, B, H, Nq, Nk):
+    """An element mask broadcastable to [B, H, Nq, Nk] (true = the key may be seen) as a contiguous
+    uint8 array of that full shape, and its pointer (None, a null pointer, for no mask)."""
+    if mask is None:
+        return None, None
+    m = np.ascontiguousarray(np.broadcast_to(np.asarray(mask).astype(bool), (B, H, Nq, Nk)), dtype=np.uint8)
+    return m, m.ctypes.data_as(_U8)
+
+
 def _shape4(q, k, v):
     q, k, v = _f64(q), _f64(k), _f64(v)
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
@@ -155,26 +165,29 @@ def _shape4(q, k, v):
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, nthreads: int | None = None,
-              window=None):
+              window=None, mask=None):
     """O = softmax(scale*QK^T + mask) V and L = m + log l for every row, by definition.
 
     q: [B,H,Nq,d], k,v: [B,H,Nk,d] (any float dtype; computed in fp64).  Masks are bottom-right
-    aligned bands (see band()); causal: row i sees key j iff j <= i + Nk - Nq.  A row with no
-    visible key gets o = 0 and lse = -inf.  Returns (o [B,H,Nq,d], lse [B,H,Nq]) as float64.
+    aligned bands (see band()); causal: row i sees key j iff j <= i + Nk - Nq.  `mask`, when given,
+    is an element mask broadcastable to [B,H,Nq,Nk] (true = visible) applied on top of the band.  A
+    row with no visible key gets o = 0 and lse = -inf.  Returns (o [B,H,Nq,d], lse [B,H,Nq]) as
+    float64.
     """
     q, k, v, B, H, Nq, Nk, d = _shape4(q, k, v)
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     wl, wr = band(causal, window)
+    m, mp = _mask_u8(mask, B, H, Nq, Nk)
     o = np.empty((B, H, Nq, d), dtype=np.float64)
     lse = np.empty((B, H, Nq), dtype=np.float64)
-    _load().oracle_attention(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d, wl, wr,
+    _load().oracle_attention(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d, wl, wr, mp,
                              float(scale), nthreads or default_threads())
     return o, lse
 
 
 def attention_rows(q, k, v, rows, causal: bool = False, scale: float | None = None,
-                   nthreads: int | None = None, window=None):
+                   nthreads: int | None = None, window=None, mask=None):
     """The same definition for selected flat row indices r = (b*H + h)*Nq + i.
 
     Returns (o [len(rows), d], lse [len(rows)]).
@@ -188,14 +201,17 @@ def attention_rows(q, k, v, rows, causal: bool = False, scale: float | None = No
     o = np.empty((rows.size, d), dtype=np.float64)
     lse = np.empty((rows.size,), dtype=np.float64)
     wl, wr = band(causal, window)
+    m, mp = _mask_u8(mask, B, H, Nq, Nk)
     _load().oracle_attention_rows(_p(q), _p(k), _p(v), rows.ctypes.data_as(_I64), rows.size,
-                                  _p(o), _p(lse), B, H, Nq, Nk, d, wl, wr, float(scale),
+                                  _p(o), _p(lse), B, H, Nq, Nk, d, wl, wr, mp, float(scale),
                                   nthreads or default_threads())
     return o, lse
 
 
-def attention_probs(q, k, causal: bool = False, scale: float | None = None, window=None) -> np.ndarray:
-    """P = softmax(scale*QK^T + mask) for one head; q [Nq,d], k [Nk,d] -> [Nq,Nk]."""
+def attention_probs(q, k, causal: bool = False, scale: float | None = None, window=None,
+                    mask=None) -> np.ndarray:
+    """P = softmax(scale*QK^T + mask) for one head; q [Nq,d], k [Nk,d] -> [Nq,Nk]; `mask` an
+    element mask broadcastable to [Nq, Nk] on top of the band."""
     q, k = _f64(q), _f64(k)
     Nq, d = q.shape
     Nk = k.shape[0]
@@ -203,12 +219,13 @@ def attention_probs(q, k, causal: bool = False, scale: float | None = None, wind
         scale = 1.0 / np.sqrt(d)
     p = np.empty((Nq, Nk), dtype=np.float64)
     wl, wr = band(causal, window)
-    _load().oracle_attention_probs(_p(q), _p(k), Nq, Nk, d, wl, wr, float(scale), _p(p))
+    m, mp = _mask_u8(mask, 1, 1, Nq, Nk)
+    _load().oracle_attention_probs(_p(q), _p(k), Nq, Nk, d, wl, wr, mp, float(scale), _p(p))
     return p
 
 
 def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = None,
-                       nthreads: int | None = None, window=None):
+                       nthreads: int | None = None, window=None, mask=None):
     """Gradients (dq, dk, dv) of O = softmax(scale*QK^T + mask) V for an upstream gradient do,
     by definition ("Flash Attention: The Hidden Gem", Phase 2), with the factor scale on dq and dk
     from X = scale * Q K^T.  Shapes as in attention(); returns float64 arrays."""
@@ -222,6 +239,7 @@ def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = 
     dk = np.empty_like(k)
     dv = np.empty_like(v)
     wl, wr = band(causal, window)
+    m, mp = _mask_u8(mask, B, H, Nq, Nk)
     _load().oracle_attention_backward(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv), B, H, Nq, Nk, d,
-                                      wl, wr, float(scale), nthreads or default_threads())
+                                      wl, wr, mp, float(scale), nthreads or default_threads())
     return dq, dk, dv

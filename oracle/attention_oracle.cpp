@@ -48,16 +48,18 @@ inline bool visible(int64_t i, int64_t j, int64_t Nq, int64_t Nk, int64_t wl, in
 //   l   = sum_j exp(x_j - m)          (pass 2)
 //   o   = sum_j exp(x_j - m) / l * v_j  (pass 3)
 //   lse = m + log(l)                  ([FA-GEM] step 6: L = m + log(l))
-// Masked keys are excluded outright (their weight is exactly zero).  Returns the number of
-// visible keys.  With none visible the max is -inf and -inf minus -inf is undefined ([FA-UND]
+// Masked keys are excluded outright (their weight is exactly zero).  `mrow`, when given, is an
+// element mask for this row over the Nk keys (nonzero = the key may be seen), applied on top of the
+// band: a mask is elementwise and independent of the scores ([FA-UND] "Attention").  Returns the
+// number of visible keys.  With none visible the max is -inf and -inf minus -inf is undefined ([FA-UND]
 // "What is left to the implementation", point 2); such a row gets no weight anywhere: o = 0 and
 // lse = log(0) = -inf (this file's reading).
 int64_t attention_row(const double* q, const double* k, const double* v, int64_t i, int64_t Nq,
-                      int64_t Nk, int64_t d, int64_t wl, int64_t wr, double scale, double* x_scratch,
-                      double* o, double* lse) {
+                      int64_t Nk, int64_t d, int64_t wl, int64_t wr, const uint8_t* mrow, double scale,
+                      double* x_scratch, double* o, double* lse) {
     int64_t nvis = 0;
     for (int64_t j = 0; j < Nk; ++j) {
-        if (!visible(i, j, Nq, Nk, wl, wr)) {
+        if (!visible(i, j, Nq, Nk, wl, wr) || (mrow != nullptr && mrow[j] == 0)) {
             x_scratch[j] = kNegInf;
             continue;
         }
@@ -161,11 +163,12 @@ void oracle_online_normalizer(const double* x, int64_t n, double* g_out, double*
 // ([FA-GEM] "Background" and step 6; [FA-UND] "Attention" for the [N,D]/[M,D] shapes and the
 // note that batch and heads only repeat independent problems).
 //   q: [B,H,Nq,d], k,v: [B,H,Nk,d], o: [B,H,Nq,d], lse: [B,H,Nq]; all row-major fp64.
-// The mask is the band (window_left, window_right) described at visible().  Returns the number of
-// rows that had no visible key.
+// The mask is the band (window_left, window_right) described at visible(), and, when `mask` is not
+// null, also the element mask [B*H][Nq][Nk] (uint8, nonzero = visible).  Returns the number of rows
+// that had no visible key.
 int64_t oracle_attention(const double* q, const double* k, const double* v, double* o, double* lse,
                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int64_t window_left,
-                         int64_t window_right, double scale, int nthreads) {
+                         int64_t window_right, const uint8_t* mask, double scale, int nthreads) {
     const int64_t rows = B * H * Nq;
     std::vector<int64_t> empty(static_cast<size_t>(std::max<int64_t>(rows, 1)), 0);
     parallel_for(rows, nthreads, [&](int64_t r) {
@@ -173,7 +176,8 @@ int64_t oracle_attention(const double* q, const double* k, const double* v, doub
         xs.resize(static_cast<size_t>(Nk));
         const int64_t bh = r / Nq, i = r % Nq;
         const int64_t n = attention_row(q + r * d, k + bh * Nk * d, v + bh * Nk * d, i, Nq, Nk, d,
-                                        window_left, window_right, scale, xs.data(), o + r * d, lse + r);
+                                        window_left, window_right, mask ? mask + r * Nk : nullptr, scale,
+                                        xs.data(), o + r * d, lse + r);
         empty[static_cast<size_t>(r)] = (n == 0);
     });
     int64_t n_empty = 0;
@@ -187,7 +191,7 @@ int64_t oracle_attention(const double* q, const double* k, const double* v, doub
 int64_t oracle_attention_rows(const double* q, const double* k, const double* v, const int64_t* rows,
                               int64_t nrows, double* o_rows, double* lse_rows, int64_t B, int64_t H,
                               int64_t Nq, int64_t Nk, int64_t d, int64_t window_left,
-                              int64_t window_right, double scale, int nthreads) {
+                              int64_t window_right, const uint8_t* mask, double scale, int nthreads) {
     (void)B;
     (void)H;
     std::vector<int64_t> empty(static_cast<size_t>(std::max<int64_t>(nrows, 1)), 0);
@@ -197,8 +201,8 @@ int64_t oracle_attention_rows(const double* q, const double* k, const double* v,
         const int64_t r = rows[n];
         const int64_t bh = r / Nq, i = r % Nq;
         const int64_t cnt = attention_row(q + r * d, k + bh * Nk * d, v + bh * Nk * d, i, Nq, Nk, d,
-                                          window_left, window_right, scale, xs.data(), o_rows + n * d,
-                                          lse_rows + n);
+                                          window_left, window_right, mask ? mask + r * Nk : nullptr, scale,
+                                          xs.data(), o_rows + n * d, lse_rows + n);
         empty[static_cast<size_t>(n)] = (cnt == 0);
     });
     int64_t n_empty = 0;
@@ -208,14 +212,16 @@ int64_t oracle_attention_rows(const double* q, const double* k, const double* v,
 
 // The probability matrix of one head, P = softmax(scale * Q K^T + mask), row by row with the
 // same three passes ([FA-GEM] "Why is Flash Attention needed?", steps 1-2).  p: [Nq, Nk];
-// masked entries are exactly 0, and so is every entry of a row with no visible key.
+// masked entries are exactly 0, and so is every entry of a row with no visible key.  `mask`, when
+// not null, is the head's element mask [Nq][Nk] (nonzero = visible), on top of the band.
 void oracle_attention_probs(const double* q, const double* k, int64_t Nq, int64_t Nk, int64_t d,
-                            int64_t window_left, int64_t window_right, double scale, double* p) {
+                            int64_t window_left, int64_t window_right, const uint8_t* mask, double scale,
+                            double* p) {
     std::vector<double> xs(static_cast<size_t>(Nk));
     for (int64_t i = 0; i < Nq; ++i) {
         double m = kNegInf;
         for (int64_t j = 0; j < Nk; ++j) {
-            if (!visible(i, j, Nq, Nk, window_left, window_right)) {
+            if (!visible(i, j, Nq, Nk, window_left, window_right) || (mask != nullptr && mask[i * Nk + j] == 0)) {
                 xs[j] = kNegInf;
                 continue;
             }
@@ -242,11 +248,12 @@ void oracle_attention_probs(const double* q, const double* k, int64_t Nq, int64_
 // the factor scale on dQ and dK is the chain rule through X = scale * Q K^T.
 //   q, dq: [B,H,Nq,d]; k, v, dk, dv: [B,H,Nk,d]; do_: [B,H,Nq,d]; fp64, row-major.
 // Heads are independent and run in parallel.  Masked entries have P = 0, hence dX = 0; a row with
-// no visible key has P = 0 throughout and gets dQ = 0.
+// no visible key has P = 0 throughout and gets dQ = 0.  `mask`, when not null, is the element mask
+// [B*H][Nq][Nk] (nonzero = visible), on top of the band.
 void oracle_attention_backward(const double* q, const double* k, const double* v, const double* do_,
                                double* dq, double* dk, double* dv, int64_t B, int64_t H, int64_t Nq,
                                int64_t Nk, int64_t d, int64_t window_left, int64_t window_right,
-                               double scale, int nthreads) {
+                               const uint8_t* mask, double scale, int nthreads) {
   parallel_for(B * H, nthreads, [&](int64_t bh) {
     const double* Q = q + bh * Nq * d;
     const double* K = k + bh * Nk * d;
@@ -256,7 +263,8 @@ void oracle_attention_backward(const double* q, const double* k, const double* v
     double* dK = dk + bh * Nk * d;
     double* dV = dv + bh * Nk * d;
     std::vector<double> P(static_cast<size_t>(Nq * Nk));
-    oracle_attention_probs(Q, K, Nq, Nk, d, window_left, window_right, scale, P.data());
+    oracle_attention_probs(Q, K, Nq, Nk, d, window_left, window_right, mask ? mask + bh * Nq * Nk : nullptr,
+                           scale, P.data());
     for (int64_t x = 0; x < Nk * d; ++x) {
       dK[x] = 0.0;
       dV[x] = 0.0;
