@@ -80,6 +80,17 @@ def visible_pairs(N, window_left=-1):
 # scheduler) and the GB300's maximum SM clock
 EX2_PER_CLOCK_PER_SM = 32
 MAX_SM_HZ = 2070e6
+# Clock-based dense bf16 rate of one SM's tensor core (8192 FLOP per clock, tcgen05 M = 128 at full
+# rate, measured by a microbenchmark) and the nominal HBM3e bandwidth: the second denominators the
+# line reports beside the measured peaks (a copy and cuBLAS stop short of both).
+TENSOR_FLOP_PER_CLOCK_PER_SM = 8192
+NOMINAL_HBM_GBS = 7900.0
+
+
+def clock_tensor_peak_tflops():
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return TENSOR_FLOP_PER_CLOCK_PER_SM * sms * MAX_SM_HZ / 1e12
 
 
 def sfu_roofline(P, window_left, ms):
@@ -481,6 +492,8 @@ def run_ours(args):
             "bound": "tensor", "achieved": round(per_launch, 2), "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": round(per_launch / peaks["bf16_tflops"], 4),
             "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM)",
+            "frac_of_clock_peak": round(per_launch / clock_tensor_peak_tflops(), 4),
+            "clock_peak": round(clock_tensor_peak_tflops(), 1),
             "traffic": recorded_traffic("prefill"),
             "algorithmic_bytes": prefill_bytes(P["B"], P["H"], P["N"], P["d"]),
             "secondary": sfu_roofline(P, args.window, pre_avg),
@@ -497,6 +510,7 @@ def run_ours(args):
             "kernel": "decode_split_kernel<128> + decode_combine_kernel<128> (fattn_decode)",
             "bound": "hbm", "achieved": round(dec_bw, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(dec_bw / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} copy bandwidth",
+            "frac_of_nominal_hbm": round(dec_bw / NOMINAL_HBM_GBS, 4), "nominal_hbm": NOMINAL_HBM_GBS,
             "traffic": recorded_traffic("decode"),
             "algorithmic_bytes": decode_bytes(D["B"], D["H"], D["Nk"], D["d"]),
         }
@@ -505,6 +519,26 @@ def run_ours(args):
         line["roofline"] = rd
     if args.configs and do_prefill and window is None and rank == 0:
         line["configs_measured"] = measure_configs(fa, dev, stream, peaks)
+    if args.configs and do_decode and rank == 0:
+        # the decode with one partial state per 64-key block, the split the workload describes
+        ws256 = torch.empty(fa.fattn_decode_workspace_size(D["B"], D["H"], D["Nk"], D["d"], 256), dtype=torch.uint8,
+                            device=dev)
+        ts = []
+        for i in range(8):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fa.fattn_decode(dq, dk, dv, scale=scale_d, num_splits=256, workspace=ws256, out=do, lse=dlse, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms256 = statistics.median(ts[2:])
+        bw256 = decode_bytes(D["B"], D["H"], D["Nk"], D["d"]) / (ms256 * 1e-3) / 1e9
+        line.setdefault("configs_measured", []).append(
+            {"workload": name_d + " one partial state per 64-key block (num_splits 256)", "ms": round(ms256, 4),
+             "gbs": round(bw256, 1), "frac": round(bw256 / peaks["hbm_gbs"], 4),
+             "frac_of_nominal_hbm": round(bw256 / NOMINAL_HBM_GBS, 4),
+             "method": "CUDA events per call, median of 6 after 2 warm calls (the 8 GiB cache exceeds L2)"})
+        del ws256
     if args.rising and do_prefill and window is None and rank == 0:
         line["prefill_rising_scores"] = measure_rising_scores(fa, dev, stream, P, pre_avg, peaks)
     if args.cpu_budget > 0:

@@ -21,6 +21,9 @@ __all__ = [
     "fattn_bwd_masked",
     "fattn_bwd_workspace_size",
     "fattn_fwd_masked",
+    "fattn_mask_row_words",
+    "fattn_mask_workspace_size",
+    "pack_mask",
     "fattn_decode",
     "fattn_decode_masked",
     "fattn_decode_static",
@@ -64,6 +67,13 @@ def lib() -> ctypes.CDLL:
     L.fattn_fwd.restype = i
     L.fattn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.fattn_fwd_masked.restype = i
+    ll = ctypes.c_longlong
+    L.fattn_mask_row_words.argtypes = [i]
+    L.fattn_mask_row_words.restype = i
+    L.fattn_mask_workspace_size.argtypes = [i, i, i, i]
+    L.fattn_mask_workspace_size.restype = sz
+    L.fattn_fwd_mask.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp, ll, ll, i, i, f, vp, sz, vp]
+    L.fattn_fwd_mask.restype = i
     L.fattn_bwd_workspace_size.argtypes = [i, i, i, i]
     L.fattn_bwd_workspace_size.restype = sz
     L.fattn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, sz, vp]
@@ -129,13 +139,37 @@ def _check(t, name, dtype=None):
         raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
 
 
+def fattn_mask_row_words(Nk: int) -> int:
+    return lib().fattn_mask_row_words(int(Nk))
+
+
+def fattn_mask_workspace_size(B: int, H: int, Nq: int, Nk: int) -> int:
+    return lib().fattn_mask_workspace_size(int(B), int(H), int(Nq), int(Nk))
+
+
+def pack_mask(mask):
+    """A boolean mask [..., Nq, Nk] (true = the key may be seen) in the library's bit layout: int32
+    words [..., Nq, fattn_mask_row_words(Nk)], key j in bit j & 31 of word j >> 5 (the 32-bit pattern
+    is what matters; int32 is only torch's carrier for it)."""
+    import torch
+    Nk = mask.shape[-1]
+    W = 4 * ((Nk + 127) // 128)
+    m = torch.nn.functional.pad(mask.to(torch.bool), (0, W * 32 - Nk))
+    m = m.reshape(*m.shape[:-1], W, 32).to(torch.int64)
+    words = (m << torch.arange(32, dtype=torch.int64, device=m.device)).sum(-1)
+    return torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32).contiguous()
+
+
 def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-              stream=None, want_lse: bool = True, window=None):
+              stream=None, want_lse: bool = True, window=None, mask=None, mask_workspace=None):
     """O = softmax(scale * Q K^T + mask) V and L per row, via the fused sm_103a kernel.
 
     q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; d in {64, 128}.  Causal masking is bottom-right
     aligned.  ``window=(window_left, window_right)`` selects a banded mask instead (fattn_fwd_masked;
-    -1 = unbounded side).  Returns (out bf16 [B,H,Nq,d], lse fp32 [B,H,Nq] or None).
+    -1 = unbounded side).  ``mask`` adds an element mask (fattn_fwd_mask): int32 words from pack_mask,
+    shaped [Nq, W], [B or 1, H or 1, Nq, W] (a dimension of 1 is shared); ``mask_workspace`` a CUDA
+    uint8 tensor of fattn_mask_workspace_size bytes (allocated here if omitted).
+    Returns (out bf16 [B,H,Nq,d], lse fp32 [B,H,Nq] or None).
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -155,6 +189,25 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if lse is not None:
         _check(lse, "lse", torch.float32)
+    if mask is not None:
+        _check(mask, "mask", torch.int32)
+        W = fattn_mask_row_words(Nk)
+        m4 = mask.reshape(1, 1, *mask.shape) if mask.dim() == 2 else mask
+        if m4.dim() != 4 or m4.shape[2:] != (Nq, W) or m4.shape[0] not in (1, B) or m4.shape[1] not in (1, H):
+            raise ValueError(f"mask must be [Nq, {W}] or [B|1, H|1, Nq, {W}] int32 words; got {tuple(mask.shape)}")
+        sb = m4.shape[1] * Nq * W if m4.shape[0] > 1 else 0
+        sh = Nq * W if m4.shape[1] > 1 else 0
+        need = fattn_mask_workspace_size(B, H, Nq, Nk)
+        if mask_workspace is None:
+            mask_workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        wl, wr = (int(window[0]), int(window[1])) if window is not None else ((-1, 0) if causal else (-1, -1))
+        st = lib().fattn_fwd_mask(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, mask.data_ptr(),
+                                  sb, sh, wl, wr, float(scale), mask_workspace.data_ptr(), mask_workspace.numel(),
+                                  _stream_handle(stream, q.device))
+        if st != FATTN_OK:
+            raise FattnError(st, "fattn_fwd_mask")
+        return out, lse
     if window is not None:
         st = lib().fattn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                     lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d,

@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libfattn.so")
 STAMP = os.path.join(BUILD, "libfattn.stamp")
 
 SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "prefill_fp8_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu",
-           "host_staging.cu"]
+           "host_staging.cu", "mask_tiles_sm103a.cu"]
 HEADERS = ["fattn_internal.h", "sm103a_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -188,8 +188,20 @@ const char* fattn_status_string(int status) {
 namespace fattn {
 namespace {
 
+// Element-mask bytes of the tile summary: one per (head, 128-row query tile, 128-key tile).
+size_t mask_tiles_bytes(int B, int H, int Nq, int Nk) {
+  return align_up(static_cast<size_t>(B) * H * ((Nq + 127) / 128) * ((Nk + 127) / 128), 256);
+}
+
+struct MaskArg {
+  const void* mask = nullptr;  // null: no element mask
+  long long sb = 0, sh = 0;
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
+};
+
 fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-                      int Nk, int d, int wl, int wr, float scale, void* stream) {
+                      int Nk, int d, int wl, int wr, float scale, void* stream, const MaskArg& mk = MaskArg()) {
   if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
@@ -209,6 +221,16 @@ fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, floa
   if (device_status_ptr(&status) != cudaSuccess || recomputed_rows_ptr(&recomputed) != cudaSuccess)
     return FATTN_ERR_CUDA;
   FwdProblem p{q, k, v, o, lse, B, H, Nq, Nk, d, wl, wr, scale, test_drop_kv_block(), recomputed};
+  if (mk.mask != nullptr) {
+    p.mask = mk.mask;
+    p.mask_sb = mk.sb;
+    p.mask_sh = mk.sh;
+    p.mask_words = fattn_mask_row_words(Nk);
+    p.tiles = static_cast<const uint8_t*>(mk.workspace);
+    if (launch_mask_tiles(static_cast<const uint32_t*>(mk.mask), mk.sb, mk.sh, p.mask_words, B, H, Nq, Nk,
+                          static_cast<uint8_t*>(mk.workspace), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return FATTN_ERR_CUDA;
+  }
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
@@ -268,6 +290,37 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
 fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                               int Nq, int Nk, int d, int window_left, int window_right, float scale, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, window_left, window_right, scale, stream);
+}
+
+int fattn_mask_row_words(int Nk) {
+  if (Nk < 1) return -1;
+  return 4 * ((Nk + 127) / 128);
+}
+
+size_t fattn_mask_workspace_size(int B, int H, int Nq, int Nk) {
+  if (!positive_sizes(B, H, Nq, Nk)) return 0;
+  return mask_tiles_bytes(B, H, Nq, Nk);
+}
+
+fattn_status fattn_fwd_mask(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                            int Nk, int d, const void* mask, long long mask_stride_b, long long mask_stride_h,
+                            int window_left, int window_right, float scale, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (mask == nullptr || !aligned16(mask) || workspace == nullptr) return FATTN_ERR_INVALID_ARG;
+  if (mask_stride_b < 0 || mask_stride_h < 0 || (mask_stride_b & 3) || (mask_stride_h & 3))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nq, Nk)) return FATTN_ERR_INVALID_ARG;
+  const size_t need = fattn_mask_workspace_size(B, H, Nq, Nk);
+  if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * ((Nq + 127) / 128) * ((Nk + 127) / 128) / 8 > 0x7fffffffLL)
+    return FATTN_ERR_INVALID_ARG;
+  MaskArg mk;
+  mk.mask = mask;
+  mk.sb = mask_stride_b;
+  mk.sh = mask_stride_h;
+  mk.workspace = workspace;
+  mk.workspace_bytes = workspace_bytes;
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, window_left, window_right, scale, stream, mk);
 }
 
 size_t fattn_bwd_workspace_size(int B, int H, int Nq, int d) {

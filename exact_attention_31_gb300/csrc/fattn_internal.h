@@ -27,8 +27,15 @@ struct FwdProblem {
   // Failure-detection testing only (never set in normal use): the key tile of this block index is
   // not loaded, so the waits for it must give up and report a timeout.  -1 = off.
   int drop_kv_block;
-  // Device counter of rows recomputed on the exact per-row path (incremented by the kernel).
+  // Device counter of rows that failed the fixed-reference range check (incremented by the kernel).
   unsigned long long* recomputed;
+  // Element mask (null: none).  Bit j & 31 of word (j >> 5) of row i of head (b, h) at
+  // mask + b * mask_sb + h * mask_sh + i * mask_words (32-bit words), set = visible.  `tiles` is its
+  // summary per 128 x 128 tile of each head, as written by launch_mask_tiles.
+  const void* mask = nullptr;
+  long long mask_sb = 0, mask_sh = 0;
+  int mask_words = 0;
+  const uint8_t* tiles = nullptr;
 };
 
 struct DecodeProblem {
@@ -79,6 +86,12 @@ cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUt
                            cudaStream_t stream);
 
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+
+// Element-mask summary: tiles[(bh * ceil(Nq / 128) + i) * ceil(Nk / 128) + j] = 0 when no bit of the
+// 128 x 128 tile (query rows 128 i.., keys 128 j.., inside Nq x Nk) of head bh is set, 2 when all
+// are, 1 otherwise.  Mask layout as in FwdProblem.
+cudaError_t launch_mask_tiles(const uint32_t* mask, long long mask_sb, long long mask_sh, int mask_words, int B,
+                              int H, int Nq, int Nk, uint8_t* tiles, cudaStream_t stream);
 
 // Backward: q, k, v, dout as for the prefill; tdq describes ws_dq as a 3-D [B*H][Nq_pad][d] fp32
 // tensor with 32-element (128-byte) inner boxes of 128 rows and 128-byte swizzle.

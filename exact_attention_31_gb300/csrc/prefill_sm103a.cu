@@ -114,7 +114,7 @@ struct Cfg {
 struct Args {
   __nv_bfloat16* o;
   float* lse;
-  int BH, Nq, Nk;
+  int BH, H, Nq, Nk;
   int wl, wr, off;     // mask band: key j visible to row i iff i+off-wl <= j <= i+off+wr (-1 = unbounded)
   int units_per_head;  // ceil(Nq / 256)
   int unit_base;       // this launch works on units [unit_base, unit_end) of the BH * units_per_head
@@ -124,6 +124,14 @@ struct Args {
   unsigned long long* recomputed;  // rows that failed the range check (diagnostic counter)
   unsigned long long timeout_ns;
   int drop_kv_block;  // failure-detection testing only; -1 = off
+  // Element mask (masked instantiation only): bit j & 31 of word (j >> 5) of row i of head (b, h) at
+  // mask + b * mask_sb + h * mask_sh + i * mask_words, set = visible; tiles[(bh * tiles_q + i / 128)
+  // * tiles_k + j / 128] = 0 when no bit of that 128 x 128 tile is set, 1 when some are, 2 when all are.
+  const uint32_t* mask;
+  long long mask_sb, mask_sh;
+  int mask_words;
+  const uint8_t* tiles;
+  int tiles_q, tiles_k;
 };
 
 // Key/value tiles [jb, je) that query tile [r0, r0 + 128) must visit: those holding a key visible to
@@ -165,6 +173,42 @@ struct Unit {
 // The k-th unit of this CTA.  The grid is persistent (at most one CTA per SM); units are taken in
 // rounds of gridDim.x, heaviest causal units (last query rows) first, and every other round is
 // walked backwards so that each CTA's total is closer to the others'.  Returns false past the end.
+// Under an element mask, 0 (no visible key), 1 (some) or 2 (all) for key tile j of query tile t.
+__device__ __forceinline__ int tile_state(const Args& a, const Unit& u, int t, int j) {
+  return a.tiles[(static_cast<size_t>(u.bh) * a.tiles_q + (u.row0 / kBlockM + t)) * a.tiles_k + j];
+}
+
+// Whether query tile t of the unit computes key tile j: inside its range and, under an element mask,
+// not a tile the mask leaves empty.
+template <bool M>
+__device__ __forceinline__ bool live(const Args& a, const Unit& u, int t, int j) {
+  if (!(u.jb[t] <= j && j < u.je[t])) return false;
+  if constexpr (M) return tile_state(a, u, t, j) != 0;
+  return true;
+}
+
+// The key tile after j that either query tile of the unit computes (J1 when none is left).
+template <bool M>
+__device__ __forceinline__ int next_live(const Args& a, const Unit& u, int j, int J1) {
+  ++j;
+  if constexpr (M) {
+    while (j < J1 && !live<M>(a, u, 0, j) && !live<M>(a, u, 1, j)) ++j;
+  }
+  return j;
+}
+
+// Key tiles query tile t of the unit computes.
+template <bool M>
+__device__ __forceinline__ int live_count(const Args& a, const Unit& u, int t) {
+  if constexpr (M) {
+    int n = 0;
+    for (int j = u.jb[t]; j < u.je[t]; ++j) n += tile_state(a, u, t, j) != 0;
+    return n;
+  }
+  return u.je[t] - u.jb[t];
+}
+
+template <bool M>
 __device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = a.unit_base + static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
@@ -174,6 +218,18 @@ __device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
   u.row0 = (a.units_per_head - 1 - i / a.BH) * kTiles * kBlockM;
   key_tiles(u.row0, a, u.jb[0], u.je[0]);
   key_tiles(u.row0 + kBlockM, a, u.jb[1], u.je[1]);
+  if constexpr (M) {
+    // Narrow each range to its first and last key tile with a visible key; a tile left with none
+    // is empty (its rows get o = 0 and L = -inf).
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+      int b = u.jb[t], e = u.je[t];
+      while (b < e && tile_state(a, u, t, b) == 0) ++b;
+      while (e > b && tile_state(a, u, t, e - 1) == 0) --e;
+      u.jb[t] = b < e ? b : 0;
+      u.je[t] = b < e ? e : 0;
+    }
+  }
   return true;
 }
 
@@ -322,7 +378,7 @@ __device__ __forceinline__ float max128_tree(const uint32_t (&s)[4][32]) {
 // stays below 2^kRescaleLog2.  With kRescaleLog2 = 0 the row's largest weight is exactly 1, which
 // bf16 holds exactly: the rows that land here are the ones whose large weights come late, and a
 // rounded dominant weight would bias their O by up to 2^-9 of its size.
-template <int D, bool kRunning>
+template <int D, bool M, bool kRunning>
 __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
                                              uint32_t sbar, const Args& a, const Abort& ab, int& g, int& done) {
   using C = Cfg<D>;
@@ -343,8 +399,23 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
   float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
   float l = 0.f;            // sum of the fp32 weights: O = O / l, L = m + log(l)
   bool ok = true;
+  // Element mask: this tile's row of tile states and this row's mask words (rows past Nq read none).
+  const uint8_t* states = nullptr;
+  const uint32_t* mrow = nullptr;
+  if constexpr (M) {
+    states = a.tiles + (static_cast<size_t>(bh) * a.tiles_q + row0 / kBlockM + t) * a.tiles_k;
+    if (q_row < a.Nq)
+      mrow = a.mask + (bh / a.H) * a.mask_sb + (bh % a.H) * a.mask_sh + static_cast<long long>(q_row) * a.mask_words;
+  }
+  int jm = jb;  // element mask: the key tile of this step (the tiles the mask leaves empty are skipped)
   for (int step = 0; step < n_tiles; ++step, ++g) {
-    const int j = jb + step;
+    const int j = M ? jm : jb + step;
+    uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);  // the row's 128 mask bits for key tile j
+    bool partial = false;
+    if constexpr (M) {
+      partial = states[j] == 1;  // the same for the whole tile
+      if (partial && mrow != nullptr) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + j);
+    }
     if (!warp_wait(sbar + 8 * (C::kSFull + t), g & 1, ab)) {
       ok = false;
       break;
@@ -389,6 +460,20 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
+      }
+    }
+    if constexpr (M) {
+      if (partial) {
+        const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (!((words[h] >> i) & 1u)) s[h][i] = __float_as_uint(-INFINITY);
+      }
+      if (step + 1 < n_tiles) {
+        do ++jm;
+        while (states[jm] == 0);
       }
     }
     float corr = 1.f;  // redo phase: factor for l and O when the reference moved in this step
@@ -537,39 +622,39 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
 
 // The redo phase of softmax group t (a function of its own, so that its code does not change the
 // main phase's): the marked tiles again with a running max, barrier phases continued from g, done.
-template <int D>
+template <int D, bool M>
 __device__ __noinline__ bool softmax_unit_running(int t, int k, int jb, int n_tiles, int row0, int bh, uint32_t tmem,
                                                   uint32_t sbar, const Args& a, const Abort& ab, int& g, int& done) {
-  return softmax_unit<D, true>(t, k, jb, n_tiles, row0, bh, tmem, sbar, a, ab, g, done);
+  return softmax_unit<D, M, true>(t, k, jb, n_tiles, row0, bh, tmem, sbar, a, ab, g, done);
 }
 
-template <int D>
+template <int D, bool M>
 __device__ __noinline__ void softmax_tail(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab, int g,
                                           int done, uint32_t* redo, bool ok) {
   if (!redo_begin(ok, ab.flag)) return;
   Unit u;
-  for (int k = 0; cta_unit(k, a, u); ++k) {
+  for (int k = 0; cta_unit<M>(k, a, u); ++k) {
     if (!redo_unit(k, redo, u) || u.je[t] == u.jb[t]) continue;
     ab.renew(a.timeout_ns);
-    if (!softmax_unit_running<D>(t, k, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done))
+    if (!softmax_unit_running<D, M>(t, k, u.jb[t], live_count<M>(a, u, t), u.row0, u.bh, tmem, sbar, a, ab, g, done))
       return;
   }
 }
 
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab,
                                              uint32_t* redo) {
   int g = 0, done = 0;
   bool ok = true;
   Unit u;
-  for (int k = 0; cta_unit(k, a, u); ++k) {
+  for (int k = 0; cta_unit<M>(k, a, u); ++k) {
     ab.renew(a.timeout_ns);
-    if (!softmax_unit<D, false>(t, k, u.jb[t], u.je[t] - u.jb[t], u.row0, u.bh, tmem, sbar, a, ab, g, done)) {
+    if (!softmax_unit<D, M, false>(t, k, u.jb[t], live_count<M>(a, u, t), u.row0, u.bh, tmem, sbar, a, ab, g, done)) {
       ok = false;
       break;
     }
   }
-  softmax_tail<D>(t, tmem, sbar, a, ab, g, done, redo, ok);
+  softmax_tail<D, M>(t, tmem, sbar, a, ab, g, done, redo, ok);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -584,7 +669,7 @@ struct ProducerState {
 
 // One unit's loads: Q of its non-empty tiles, then K_j and V_j for the union of the two tiles' ranges
 // (ring index ring + 2 (j - J0) + w).  False when a wait gave up.
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ bool producer_unit(const Unit& u, const CUtensorMap* tq, const CUtensorMap* tk,
                                               const CUtensorMap* tv, uint32_t sbase, const Args& a,
                                               const Abort& ab, ProducerState& ps) {
@@ -604,10 +689,11 @@ __device__ __forceinline__ bool producer_unit(const Unit& u, const CUtensorMap* 
     ++ps.qloads[t];
   }
   const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
-  for (int j = J0; j < J1; ++j) {
+  int n = 0;  // key tiles loaded for this unit (ring index ring + 2 n + w)
+  for (int j = J0; j < J1; j = next_live<M>(a, u, j, J1), ++n) {
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
-      const int idx = ps.ring + 2 * (j - J0) + w;
+      const int idx = ps.ring + 2 * n + w;
       const int slot = idx % C::kSlots;
       const int round = idx / C::kSlots;
       if (round > 0 && !thread_wait(sbar + 8 * (C::kKVEmpty + slot), (round - 1) & 1, ab)) return false;
@@ -624,20 +710,20 @@ __device__ __forceinline__ bool producer_unit(const Unit& u, const CUtensorMap* 
                     j * kBlockN, u.bh);
     }
   }
-  if (J1 > J0) ps.ring += 2 * (J1 - J0);
+  ps.ring += 2 * n;
   return true;
 }
 
-template <int D>
+template <int D, bool M>
 __device__ __noinline__ bool producer_unit_redo(const Unit& u, const CUtensorMap* tq, const CUtensorMap* tk,
                                                 const CUtensorMap* tv, uint32_t sbase, const Args& a, const Abort& ab,
                                                 ProducerState& ps) {
-  return producer_unit<D>(u, tq, tk, tv, sbase, a, ab, ps);
+  return producer_unit<D, M>(u, tq, tk, tv, sbase, a, ab, ps);
 }
 
 // The producer's redo phase and wind-down (whole warp; lane 0 issues).  After a wait gave up, the
 // copies already in flight land before the CTA's shared memory goes away.
-template <int D>
+template <int D, bool M>
 __device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                            uint32_t sbase, const Args& a, Abort ab, ProducerState ps, bool ok,
                                            uint32_t* redo) {
@@ -646,10 +732,10 @@ __device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensor
   const bool lead = (threadIdx.x & 31) == 0;
   if (redo_begin(ok, ab.flag) && lead) {
     Unit u;
-    for (int k = 0; cta_unit(k, a, u); ++k) {
+    for (int k = 0; cta_unit<M>(k, a, u); ++k) {
       if (!redo_unit(k, redo, u)) continue;
       ab.renew(a.timeout_ns);
-      if (!producer_unit_redo<D>(u, tq, tk, tv, sbase, a, ab, ps)) {
+      if (!producer_unit_redo<D, M>(u, tq, tk, tv, sbase, a, ab, ps)) {
         ok = false;
         break;
       }
@@ -671,7 +757,7 @@ __device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensor
 }
 
 // Whole warp; lane 0 issues the main phase's loads.
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                               uint32_t sbase, const Args& a, Abort ab, uint32_t* redo) {
   ProducerState ps;
@@ -681,16 +767,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
     tma_prefetch_desc(tk);
     tma_prefetch_desc(tv);
     Unit u;
-    for (int k = 0; cta_unit(k, a, u); ++k) {
+    for (int k = 0; cta_unit<M>(k, a, u); ++k) {
       ab.renew(a.timeout_ns);
-      if (!producer_unit<D>(u, tq, tk, tv, sbase, a, ab, ps)) {
+      if (!producer_unit<D, M>(u, tq, tk, tv, sbase, a, ab, ps)) {
         ok = false;
         break;
       }
     }
   }
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  producer_tail<D>(tq, tk, tv, sbase, a, ab, ps, ok, redo);
+  producer_tail<D, M>(tq, tk, tv, sbase, a, ab, ps, ok, redo);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -798,14 +884,38 @@ __device__ __forceinline__ bool issue_pv_step(int t, int slot, bool first, bool 
 // or not tile t uses it; a commit for a slot's next use can only follow that use's load, which
 // itself waited for both of the previous use's arrivals.  Ring index of K_j is ring + 2 (j - J0),
 // of V_j one more.
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ bool mma_unit_tile(int t, const Unit& u, const MmaCtx<D>& m, MmaState& st,
-                                              const Abort& ab) {
+                                              const Abort& ab, const Args& a) {
   using C = Cfg<D>;
   const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
   if (J0 >= J1) return true;
   const int jb = t ? u.jb[1] : u.jb[0], je = t ? u.je[1] : u.je[0];
   const int r0 = st.ring;
+  if constexpr (M) {
+    // The same schedule over the key tiles either query tile computes (n-th loaded: ring r0 + 2 n).
+    if (!m.wait_kv(r0, ab)) return false;
+    tc_fence_after();
+    if (live<M>(a, u, t, J0) && !issue_s_step<D>(t, r0 % C::kSlots, J0 == je - 1, m, st, ab)) return false;
+    m.commit(C::kKVEmpty + r0 % C::kSlots);
+    int n = 0;
+    for (int j = J0; j < J1; ++n) {
+      const int jn = next_live<M>(a, u, j, J1);
+      if (jn < J1) {
+        const int kidx = r0 + 2 * (n + 1);
+        if (!m.wait_kv(kidx, ab)) return false;
+        if (live<M>(a, u, t, jn) && !issue_s_step<D>(t, kidx % C::kSlots, jn == je - 1, m, st, ab)) return false;
+        m.commit(C::kKVEmpty + kidx % C::kSlots);
+      }
+      const int vidx = r0 + 2 * n + 1;
+      if (!m.wait_kv(vidx, ab)) return false;
+      if (live<M>(a, u, t, j) && !issue_pv_step<D>(t, vidx % C::kSlots, j == jb, j == je - 1, m, st, ab)) return false;
+      m.commit(C::kKVEmpty + vidx % C::kSlots);
+      j = jn;
+    }
+    st.ring = r0 + 2 * n;
+    return true;
+  }
   if (!m.wait_kv(r0, ab)) return false;
   tc_fence_after();
   if (jb <= J0 && J0 < je && !issue_s_step<D>(t, r0 % C::kSlots, J0 == je - 1, m, st, ab)) return false;
@@ -829,14 +939,41 @@ __device__ __forceinline__ bool mma_unit_tile(int t, const Unit& u, const MmaCtx
 
 // P aliased over S (d = 128): S_t(j+1) is issued after P_t(j) V_j, which reads P_t from the same
 // columns (tcgen05.mma operations of one CTA execute in issue order).
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D>& m, MmaState& st,
-                                                   const Abort& ab) {
+                                                   const Abort& ab, const Args& a) {
   using C = Cfg<D>;
   const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
   if (J0 >= J1) return true;
   auto active = [&](int t, int j) { return u.jb[t] <= j && j < u.je[t]; };
   const int r0 = st.ring;
+  if constexpr (M) {
+    // The same schedule over the key tiles either query tile computes: the n-th loaded tile j (ring
+    // r0 + 2 n) after the previous one jp.
+    int j = J0, jp = -1, n = 0;
+    for (;;) {
+      const int r = r0 + 2 * n;
+      if (j < J1 && !m.wait_kv(r, ab)) return false;
+      if (n > 0 && !m.wait_kv(r - 1, ab)) return false;  // V_jp
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        if (n > 0 && live<M>(a, u, t, jp) &&
+            !issue_pv_step<D>(t, (r - 1) % C::kSlots, jp == u.jb[t], jp == u.je[t] - 1, m, st, ab))
+          return false;
+        if (j < J1 && live<M>(a, u, t, j) && !issue_s_step<D>(t, r % C::kSlots, j == u.je[t] - 1, m, st, ab))
+          return false;
+      }
+      if (j < J1) m.commit(C::kKVEmpty + r % C::kSlots);
+      if (n > 0) m.commit(C::kKVEmpty + (r - 1) % C::kSlots);
+      if (j >= J1) break;
+      jp = j;
+      j = next_live<M>(a, u, j, J1);
+      ++n;
+    }
+    st.ring = r0 + 2 * n;
+    return true;
+  }
   for (int j = J0; j <= J1; ++j) {
     const int r = r0 + 2 * (j - J0);  // ring index of K_j
     if (j < J1 && !m.wait_kv(r, ab)) return false;
@@ -856,30 +993,31 @@ __device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D
   return true;
 }
 
-template <int D>
-__device__ __noinline__ bool mma_unit_redo(int tt, const Unit& u, const MmaCtx<D>& m, MmaState& st, const Abort& ab) {
+template <int D, bool M>
+__device__ __noinline__ bool mma_unit_redo(int tt, const Unit& u, const MmaCtx<D>& m, MmaState& st, const Abort& ab,
+                                           const Args& a) {
   using C = Cfg<D>;
   bool ok = true;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t)
     if ((!C::kSepP || t == tt) && u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
-  if (ok) ok = C::kSepP ? mma_unit_tile<D>(tt, u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
+  if (ok) ok = C::kSepP ? mma_unit_tile<D, M>(tt, u, m, st, ab, a) : mma_unit_aliased_p<D, M>(u, m, st, ab, a);
   return ok;
 }
 
 // The MMA warp's redo phase and wind-down: before the CTA winds down, every MMA (and every arrival
 // its commits make on this CTA's barriers) has completed, on the normal path and after a timeout
 // alike.
-template <int D>
+template <int D, bool M>
 __device__ __noinline__ void mma_tail(int tt, const MmaCtx<D>& m, MmaState st, const Args& a, Abort ab, bool ok,
                                       uint32_t* redo) {
   using C = Cfg<D>;
   if (redo_begin(ok, ab.flag)) {
     Unit u;
-    for (int k = 0; ok && cta_unit(k, a, u); ++k) {
+    for (int k = 0; ok && cta_unit<M>(k, a, u); ++k) {
       if (!redo_unit(k, redo, u)) continue;
       ab.renew(a.timeout_ns);
-      ok = mma_unit_redo<D>(tt, u, m, st, ab);
+      ok = mma_unit_redo<D, M>(tt, u, m, st, ab, a);
     }
   }
   const int drain = tt ? C::kDrain1 : C::kDrain;
@@ -892,7 +1030,7 @@ __device__ __noinline__ void mma_tail(int tt, const MmaCtx<D>& m, MmaState st, c
 
 // Whole warp.  `tt` is the query tile of this warp (d = 64); with d = 128 the one MMA warp (tt = 0)
 // issues both tiles' products.
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, const Args& a, Abort ab,
                                          uint32_t* redo) {
   using C = Cfg<D>;
@@ -901,17 +1039,17 @@ __device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, 
   MmaState st;
   bool ok = true;
   Unit u;
-  for (int k = 0; ok && cta_unit(k, a, u); ++k) {
+  for (int k = 0; ok && cta_unit<M>(k, a, u); ++k) {
     ab.renew(a.timeout_ns);
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
       if ((!C::kSepP || t == tt) && u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
-    if (ok) ok = C::kSepP ? mma_unit_tile<D>(tt, u, m, st, ab) : mma_unit_aliased_p<D>(u, m, st, ab);
+    if (ok) ok = C::kSepP ? mma_unit_tile<D, M>(tt, u, m, st, ab, a) : mma_unit_aliased_p<D, M>(u, m, st, ab, a);
   }
-  mma_tail<D>(tt, m, st, a, ab, ok, redo);
+  mma_tail<D, M>(tt, m, st, a, ab, ok, redo);
 }
 
-template <int D>
+template <int D, bool M>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Args a) {
@@ -961,13 +1099,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each role works through the CTA's units, then meets the others at one barrier (redo_begin) and
   // computes the marked tiles again.
   if (warp < 8) {
-    softmax_role<D>(warp >> 2, tmem, sbar, a, ab, redo);
+    softmax_role<D, M>(warp >> 2, tmem, sbar, a, ab, redo);
   } else if (warp == kProducerWarp) {
-    producer_role<D>(&tm_q, &tm_k, &tm_v, sbase, a, ab, redo);
+    producer_role<D, M>(&tm_q, &tm_k, &tm_v, sbase, a, ab, redo);
   } else if (warp == kMmaWarp) {
-    mma_role<D>(0, tmem, sbase, a, ab, redo);
+    mma_role<D, M>(0, tmem, sbase, a, ab, redo);
   } else if (C::kSepP && warp == kMmaWarp1) {
-    mma_role<D>(1, tmem, sbase, a, ab, redo);
+    mma_role<D, M>(1, tmem, sbase, a, ab, redo);
   } else {
     redo_begin(true, abort_flag);  // (d = 128: the spare warp only takes part in the barrier)
   }
@@ -980,7 +1118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool M>
 cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
                      cudaStream_t stream) {
@@ -990,7 +1128,7 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_kernel<D, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -999,6 +1137,7 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.lse = p.lse;
   a.BH = p.B * p.H;
+  a.H = p.H;
   a.Nq = p.Nq;
   a.Nk = p.Nk;
   a.wl = p.window_left;
@@ -1010,6 +1149,13 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.recomputed = p.recomputed;
   a.timeout_ns = timeout_ns;
   a.drop_kv_block = p.drop_kv_block;
+  a.mask = static_cast<const uint32_t*>(p.mask);
+  a.mask_sb = p.mask_sb;
+  a.mask_sh = p.mask_sh;
+  a.mask_words = p.mask_words;
+  a.tiles = p.tiles;
+  a.tiles_q = (p.Nq + kBlockM - 1) / kBlockM;
+  a.tiles_k = (p.Nk + kBlockN - 1) / kBlockN;
   // Persistent: one CTA per SM (each holds all of an SM's tensor memory), looping over the units.
   static int sm_count[64] = {};
   if (dev < 0 || dev >= 64 || sm_count[dev] == 0) {
@@ -1028,7 +1174,7 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
     a.unit_base = static_cast<int>(base);
     a.unit_end = static_cast<int>(std::min(total, base + per_launch));
     const unsigned int g = static_cast<unsigned int>(std::min<long long>(grid, a.unit_end - a.unit_base));
-    prefill_kernel<D><<<g, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+    prefill_kernel<D, M><<<g, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1040,8 +1186,12 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
 cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
                            cudaStream_t stream) {
-  if (p.d == 64) return launch_d<64>(p, tq, tk, tv, status, timeout_ns, stream);
-  return launch_d<128>(p, tq, tk, tv, status, timeout_ns, stream);
+  if (p.tiles != nullptr) {
+    if (p.d == 64) return launch_d<64, true>(p, tq, tk, tv, status, timeout_ns, stream);
+    return launch_d<128, true>(p, tq, tk, tv, status, timeout_ns, stream);
+  }
+  if (p.d == 64) return launch_d<64, false>(p, tq, tk, tv, status, timeout_ns, stream);
+  return launch_d<128, false>(p, tq, tk, tv, status, timeout_ns, stream);
 }
 
 }  // namespace fattn

@@ -88,6 +88,36 @@ fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void*
                               void* stream);
 
 /*
+ * fattn_fwd_mask -- fattn_fwd_masked with an element mask on top of the band ("Understanding
+ * FlashAttention", Attention: a mask is elementwise and independent of the scores; What is left to
+ * the implementation, point 2: rows whose keys are all masked).  O = softmax(scale * Q K^T + mask) V
+ * where the mask gives -inf to the pairs (i, j) that the band or the element mask hides.
+ *
+ *   mask      device memory, 16-byte aligned, owned by the caller: a bit per (query, key) pair.  Row
+ *             i of head (b, h) is fattn_mask_row_words(Nk) 32-bit words starting at word
+ *             b * mask_stride_b + h * mask_stride_h + i * fattn_mask_row_words(Nk); key j is bit
+ *             (j & 31) of its word j >> 5, set = the key may be seen.  Bits past Nk are ignored.
+ *   mask_stride_b, mask_stride_h   in 32-bit words, >= 0 and multiples of 4; 0 shares one mask over
+ *             that dimension (one mask for every head: mask_stride_h = 0).
+ *   window_left, window_right   the band of fattn_fwd_masked ((-1, -1) for the element mask alone).
+ *   workspace device memory of at least fattn_mask_workspace_size(B, H, Nq, Nk) bytes, owned by the
+ *             caller: it receives one byte per (head, 128-query tile, 128-key tile) telling whether the
+ *             mask hides all, some or none of that tile.  Tiles it hides entirely are skipped (no
+ *             loads, no products); only partly hidden tiles read the mask bits.  Calls sharing a
+ *             workspace must not overlap.
+ *
+ * A row with no visible key gets o = 0 and L = -inf.  Two kernels run on `stream`: the tile summary,
+ * then the forward.  Returns FATTN_ERR_INVALID_ARG for a null or misaligned mask, a negative or
+ * unaligned stride, or a short workspace; other arguments as for fattn_fwd_masked.
+ */
+int fattn_mask_row_words(int Nk); /* 4 * ceil(Nk / 128): whole 16-byte groups per row; -1 if Nk < 1 */
+size_t fattn_mask_workspace_size(int B, int H, int Nq, int Nk);
+fattn_status fattn_fwd_mask(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                            int Nk, int d, const void* mask, long long mask_stride_b, long long mask_stride_h,
+                            int window_left, int window_right, float scale, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * fattn_bwd -- gradients of the attention forward ("Flash Attention: The Hidden Gem", Phase 2:
  * Chain Rule Through a Matrix Multiply, The Softmax Jacobian, The D Shortcut, The Algorithm).
  *

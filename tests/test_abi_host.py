@@ -218,3 +218,30 @@ def test_decode_host_rejects_bad_arguments(L, change, expect):
     st = L.fattn_decode_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nk"], a["d"],
                              a["wl"], a["wr"], a["scale"], a["hpc"], a["ws"], a["ws_bytes"], None)
     assert st == expect
+
+
+def test_mask_row_words_and_workspace(L):
+    # four 32-bit words per 128 keys, so every mask row starts on 16 bytes; one summary byte per
+    # (head, 128-query tile, 128-key tile), padded to 256 bytes
+    assert L.fattn_mask_row_words(1) == 4 and L.fattn_mask_row_words(128) == 4 and L.fattn_mask_row_words(129) == 8
+    assert L.fattn_mask_row_words(0) == -1
+    assert L.fattn_mask_workspace_size(2, 3, 300, 1000) == (2 * 3 * 3 * 8 + 255) // 256 * 256
+    assert L.fattn_mask_workspace_size(1, 32, 8192, 8192) == 32 * 64 * 64
+    assert L.fattn_mask_workspace_size(1, 1, 0, 8) == 0
+
+
+@pytest.mark.parametrize("mask,sb,sh,ws,nbytes,expect", [
+    (None, 0, 0, A, 256, 1),    # no mask
+    (A + 4, 0, 0, A, 256, 1),   # misaligned mask
+    (A, -4, 0, A, 256, 1),      # negative stride
+    (A, 0, 2, A, 256, 1),       # stride not a multiple of 4 words
+    (A, 0, 0, None, 256, 1),    # no workspace
+    (A, 0, 0, A, 255, 1),       # workspace too small
+])
+def test_fwd_mask_rejects_bad_arguments(L, mask, sb, sh, ws, nbytes, expect):
+    L.fattn_fwd_mask.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_longlong,
+                                                                             ctypes.c_longlong, ctypes.c_int,
+                                                                             ctypes.c_int, ctypes.c_float,
+                                                                             ctypes.c_void_p, ctypes.c_size_t,
+                                                                             ctypes.c_void_p]
+    assert L.fattn_fwd_mask(A, A, A, A, None, 1, 1, 8, 8, 64, mask, sb, sh, -1, -1, 0.125, ws, nbytes, None) == expect
