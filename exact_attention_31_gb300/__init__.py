@@ -20,6 +20,7 @@ __all__ = [
     "fattn_bwd",
     "fattn_bwd_masked",
     "fattn_bwd_workspace_size",
+    "fattn_bwd_mask_workspace_size",
     "fattn_fwd_masked",
     "fattn_mask_row_words",
     "fattn_mask_workspace_size",
@@ -74,6 +75,10 @@ def lib() -> ctypes.CDLL:
     L.fattn_mask_workspace_size.restype = sz
     L.fattn_fwd_mask.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp, ll, ll, i, i, f, vp, sz, vp]
     L.fattn_fwd_mask.restype = i
+    L.fattn_bwd_mask_workspace_size.argtypes = [i, i, i, i, i]
+    L.fattn_bwd_mask_workspace_size.restype = sz
+    L.fattn_bwd_mask.argtypes = [vp] * 9 + [i, i, i, i, i, vp, ll, ll, i, i, f, vp, sz, vp]
+    L.fattn_bwd_mask.restype = i
     L.fattn_bwd_workspace_size.argtypes = [i, i, i, i]
     L.fattn_bwd_workspace_size.restype = sz
     L.fattn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, sz, vp]
@@ -190,13 +195,7 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     if lse is not None:
         _check(lse, "lse", torch.float32)
     if mask is not None:
-        _check(mask, "mask", torch.int32)
-        W = fattn_mask_row_words(Nk)
-        m4 = mask.reshape(1, 1, *mask.shape) if mask.dim() == 2 else mask
-        if m4.dim() != 4 or m4.shape[2:] != (Nq, W) or m4.shape[0] not in (1, B) or m4.shape[1] not in (1, H):
-            raise ValueError(f"mask must be [Nq, {W}] or [B|1, H|1, Nq, {W}] int32 words; got {tuple(mask.shape)}")
-        sb = m4.shape[1] * Nq * W if m4.shape[0] > 1 else 0
-        sh = Nq * W if m4.shape[1] > 1 else 0
+        sb, sh = _mask_strides(mask, B, H, Nq, Nk)
         need = fattn_mask_workspace_size(B, H, Nq, Nk)
         if mask_workspace is None:
             mask_workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -227,13 +226,30 @@ def fattn_bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
     return lib().fattn_bwd_workspace_size(int(B), int(H), int(Nq), int(d))
 
 
+def _mask_strides(mask, B, H, Nq, Nk):
+    """(sb, sh) in 32-bit words for a pack_mask tensor shaped [Nq, W] or [B|1, H|1, Nq, W]."""
+    import torch
+    _check(mask, "mask", torch.int32)
+    W = fattn_mask_row_words(Nk)
+    m4 = mask.reshape(1, 1, *mask.shape) if mask.dim() == 2 else mask
+    if m4.dim() != 4 or m4.shape[2:] != (Nq, W) or m4.shape[0] not in (1, B) or m4.shape[1] not in (1, H):
+        raise ValueError(f"mask must be [Nq, {W}] or [B|1, H|1, Nq, {W}] int32 words; got {tuple(mask.shape)}")
+    return (m4.shape[1] * Nq * W if m4.shape[0] > 1 else 0), (Nq * W if m4.shape[1] > 1 else 0)
+
+
+def fattn_bwd_mask_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return lib().fattn_bwd_mask_workspace_size(int(B), int(H), int(Nq), int(Nk), int(d))
+
+
 def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,
-              dv=None, workspace=None, stream=None, window=None):
+              dv=None, workspace=None, stream=None, window=None, mask=None):
     """Gradients (dq, dk, dv) of the attention forward for an upstream gradient ``dout``.
 
     q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; out (bf16) and lse (fp32 [B,H,Nq]) are the forward's
     outputs for the same inputs, mask and scale.  ``workspace`` is a CUDA uint8 tensor of at least
-    fattn_bwd_workspace_size(B, H, Nq, d) bytes (allocated here if omitted).  Returns bf16 tensors.
+    fattn_bwd_workspace_size(B, H, Nq, d) bytes (fattn_bwd_mask_workspace_size(B, H, Nq, Nk, d) with
+    ``mask``; allocated here if omitted).  ``mask`` is the element mask given to fattn_fwd
+    (fattn_bwd_mask).  Returns bf16 tensors.
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
@@ -249,7 +265,7 @@ def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None
     Nk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = fattn_bwd_workspace_size(B, H, Nq, d)
+    need = fattn_bwd_workspace_size(B, H, Nq, d) if mask is None else fattn_bwd_mask_workspace_size(B, H, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace")
@@ -258,6 +274,16 @@ def fattn_bwd(q, k, v, out, lse, dout, causal: bool = False, scale: float | None
     dv = torch.empty_like(v) if dv is None else dv
     for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, torch.bfloat16)
+    if mask is not None:
+        sb, sh = _mask_strides(mask, B, H, Nq, Nk)
+        wl, wr = _band(causal, window)
+        st = lib().fattn_bwd_mask(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                  dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                                  mask.data_ptr(), sb, sh, wl, wr, float(scale), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+        if st != FATTN_OK:
+            raise FattnError(st, "fattn_bwd_mask")
+        return dq, dk, dv
     if window is not None:
         st = lib().fattn_bwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                     dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk,

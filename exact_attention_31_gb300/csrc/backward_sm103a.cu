@@ -147,7 +147,32 @@ struct BArgs {
   int drop_kv;  // failure-detection testing only: K_j and V_j are never loaded
   int nkt;      // key tiles per head
   int group;    // heads per CTA group (1 .. BH)
+  // Element mask (masked instantiation only), laid out as for the forward: bit j & 31 of word j >> 5
+  // of query row i of head (b, h) at mask + b * mask_sb + h * mask_sh + i * mask_words, set = visible;
+  // tiles[(bh * tiles_q + i / 128) * tiles_k + j / 128] = 0 (none visible), 1 (some) or 2 (all).
+  int H;
+  const uint32_t* mask;
+  long long mask_sb, mask_sh;
+  int mask_words;
+  const uint8_t* tiles;
+  int tiles_q;
 };
+
+// Under an element mask, the state (0 none, 1 some, 2 all visible) of query tile qt against key tile jt.
+__device__ __forceinline__ int bwd_tile_state(const BArgs& a, int bh, int qt, int jt) {
+  return a.tiles[(static_cast<size_t>(bh) * a.tiles_q + qt) * a.nkt + jt];
+}
+
+// The query tile after qt (from it0 - 1 on) that this key tile computes: every one without a mask,
+// the ones the mask does not hide entirely with one.
+template <bool M>
+__device__ __forceinline__ int next_qtile(const BArgs& a, int bh, int jt, int qt) {
+  ++qt;
+  if constexpr (M) {
+    while (bwd_tile_state(a, bh, qt, jt) == 0) ++qt;
+  }
+  return qt;
+}
 
 struct Abort {
   volatile uint32_t* flag;
@@ -199,7 +224,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // ------------------------------------------------------------------------------------------------
 // Compute warps: one thread per key; each warp covers 64 of the tile's 128 queries.
 // ------------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uint32_t tmem, uint32_t sbase,
                                              const uint8_t* smem, const BArgs& a, const Abort& ab) {
   using C = BCfg<D>;
@@ -211,9 +236,11 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
   const uint32_t sbar = sbase + C::kBarOff;
   const float c = a.c_log2;
   bool ok = true;
+  int qt = it0 - 1;  // element mask: the query tile of step i
   for (int i = 0; i < n; ++i) {
     const int b = i % C::kSBufs;
     const int dsb = i % C::kDSBufs;
+    if constexpr (M) qt = next_qtile<M>(a, bh, n0 / kBN, qt);
     if (!warp_wait(sbar + 8 * (C::kSFull + b), (i / C::kSBufs) & 1, ab) ||
         !warp_wait(sbar + 8 * C::kDPFull, i & 1, ab) ||
         (!C::kTwoS && i >= C::kDSBufs && !warp_wait(sbar + 8 * (C::kDSEmpty + dsb), ((i / C::kDSBufs) - 1) & 1, ab))) {
@@ -221,7 +248,8 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
       break;
     }
     tc_fence_after();
-    const int q0 = (it0 + i) * kBM;
+    const int q0 = (M ? qt : it0 + i) * kBM;
+    const bool partial = M && bwd_tile_state(a, bh, q0 / kBM, n0 / kBN) == 1;  // the same for the whole tile
     const uint32_t tS = tmem + lane_field + C::col_s(b);
     const uint32_t tDP = tmem + lane_field + C::kColDP;
     const uint32_t ds_row = sbase + C::kDSOff + dsb * C::kDSBytes + half * kAtom + kr * 128;
@@ -246,6 +274,23 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
       const int e_lo = a.wr >= 0 ? kidx - a.off - a.wr - (q0 + qa) : -1;
       const int e_hi = a.wl >= 0 ? kidx - a.off + a.wl - (q0 + qa) : 32;
       const bool mask = __any_sync(0xffffffffu, e_lo > 0 || e_hi < 31);
+      // Element mask on a partly hidden tile: lane e loads the word of query q0 + qa + e that holds
+      // this warp's 32 keys, and 32 ballots turn those rows into columns, so that bit e of `vis` says
+      // whether this thread's key is visible to query q0 + qa + e.
+      uint32_t vis = ~0u;
+      if constexpr (M) {
+        if (partial) {
+          const int qrow = q0 + qa + lane;
+          const uint32_t word = qrow < a.Nq ? __ldg(a.mask + (bh / a.H) * a.mask_sb + (bh % a.H) * a.mask_sh +
+                                                        static_cast<long long>(qrow) * a.mask_words + (kidx >> 5))
+                                            : 0u;
+#pragma unroll
+          for (int kb = 0; kb < 32; ++kb) {
+            const uint32_t col = __ballot_sync(0xffffffffu, (word >> kb) & 1u);
+            if (lane == kb) vis = col;
+          }
+        }
+      }
       uint32_t pp[16], pd[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
@@ -256,6 +301,12 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
         if (mask) {
           p0 = (e < e_lo || e > e_hi) ? 0.f : p0;
           p1 = (e + 1 < e_lo || e + 1 > e_hi) ? 0.f : p1;
+        }
+        if constexpr (M) {
+          if (partial) {
+            p0 = ((vis >> e) & 1u) ? p0 : 0.f;
+            p1 = ((vis >> (e + 1)) & 1u) ? p1 : 0.f;
+          }
         }
         float d0, d1;
         fmul2(d0, d1, p0, p1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]));
@@ -319,7 +370,7 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
 // ------------------------------------------------------------------------------------------------
 // TMA producer (one thread)
 // ------------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool M>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                               const CUtensorMap* tdo, int n, int it0, int n0, int bh,
                                               uint32_t sbase, const BArgs& a, const Abort& ab) {
@@ -341,9 +392,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
   // is free once dK_i has read it, dO_i's once dV_i has.
   int issued = 0;
   bool ok = true;
+  int qt = it0 - 1;  // element mask: the query tile of step i
   for (int i = 0; i < n && ok; ++i) {
     const int st = i % C::kStages, use = i / C::kStages;
-    const int q0 = (it0 + i) * kBM;
+    if constexpr (M) qt = next_qtile<M>(a, bh, n0 / kBN, qt);
+    const int q0 = (M ? qt : it0 + i) * kBM;
     const size_t r0 = (static_cast<size_t>(bh) * a.Nq_pad + q0) * 16;
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
@@ -574,9 +627,9 @@ __device__ __forceinline__ void mma_role(int n, uint32_t tmem, uint32_t sbase, b
 // ------------------------------------------------------------------------------------------------
 // dQ drain warps: one thread per query row of the tile.
 // ------------------------------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it0, int bh, uint32_t tmem,
-                                           uint32_t sbase, const Abort& ab) {
+template <int D, bool M>
+__device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it0, int n0, int bh, uint32_t tmem,
+                                           uint32_t sbase, const BArgs& a, const Abort& ab) {
   using C = BCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
@@ -586,11 +639,13 @@ __device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it
   const bool issuer = (warp == kDrainWarp0) && lane == 0;
   const uint32_t stg = sbase + C::kDQOff;  // two [128 rows][32 fp32] boxes, 128-byte swizzled
   if (issuer) tma_prefetch_desc(tdq);
+  int qt = it0 - 1;  // element mask: the query tile of step i
   for (int i = 0; i < n; ++i) {
     const int b = i % C::kSBufs;
+    if constexpr (M) qt = next_qtile<M>(a, bh, n0 / kBN, qt);
     bool fail = !warp_wait(sbar + 8 * (C::kDQFull + b), (i / C::kSBufs) & 1, ab);
     if (!fail) tc_fence_after();
-    const int q0 = (it0 + i) * kBM;
+    const int q0 = (M ? qt : it0 + i) * kBM;
 #pragma unroll 1
     for (int pass = 0; pass < D / 64; ++pass) {
       uint32_t v[2][32];
@@ -630,7 +685,7 @@ __device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it
   if (issuer) bulk_wait_all();
 }
 
-template <int D>
+template <int D, bool M>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -662,7 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long q_hi = a.wl >= 0 ? min(static_cast<long long>(a.Nq) - 1, static_cast<long long>(k_last) - a.off + a.wl)
                                    : static_cast<long long>(a.Nq) - 1;
   const int it0 = q_lo <= q_hi ? static_cast<int>(q_lo / kBM) : 0;
-  const int n = q_lo <= q_hi ? static_cast<int>(q_hi / kBM) + 1 - it0 : 0;
+  int n = q_lo <= q_hi ? static_cast<int>(q_hi / kBM) + 1 - it0 : 0;
+  if constexpr (M) {
+    // Only the query tiles the element mask does not hide entirely.
+    int live = 0;
+    for (int qt = it0; qt < it0 + n; ++qt) live += bwd_tile_state(a, bh, qt, jt) != 0;
+    n = live;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(sbar + 8 * C::kKVFull, 1);
@@ -717,16 +778,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    compute_role<D>(n, it0, n0, bh, tmem, sbase, smem, a, ab);
+    compute_role<D, M>(n, it0, n0, bh, tmem, sbase, smem, a, ab);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role<D>(&tm_q, &tm_k, &tm_v, &tm_do, n, it0, n0, bh, sbase, a, ab);
+    if ((threadIdx.x & 31) == 0) producer_role<D, M>(&tm_q, &tm_k, &tm_v, &tm_do, n, it0, n0, bh, sbase, a, ab);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     mma_role<D>(n, tmem, sbase, false, ab);
   } else if (warp == kSWarp) {
     if (C::kTwoS) mma_role<D>(n, tmem, sbase, true, ab);
   } else {
-    drain_role<D>(&tm_dq, n, it0, bh, tmem, sbase, ab);
+    drain_role<D, M>(&tm_dq, n, it0, n0, bh, tmem, sbase, a, ab);
   }
 
   tc_fence_before();
@@ -824,7 +885,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
   *reinterpret_cast<uint4*>(dq + static_cast<size_t>(r) * D + 8 * g) = out;
 }
 
-template <int D>
+template <int D, bool M>
 cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdq, unsigned int* status,
                          unsigned long long timeout_ns, cudaStream_t stream) {
@@ -834,7 +895,7 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(bwd_kernel<D, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -871,6 +932,13 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
   a.timeout_ns = timeout_ns;
   a.drop_kv = p.drop_kv;
   a.nkt = (p.Nk + kBN - 1) / kBN;
+  a.H = p.H;
+  a.mask = static_cast<const uint32_t*>(p.mask);
+  a.mask_sb = p.mask_sb;
+  a.mask_sh = p.mask_sh;
+  a.mask_words = p.mask_words;
+  a.tiles = p.tiles;
+  a.tiles_q = (p.Nq + kBM - 1) / kBM;
   {
     // Heads per group: as many as keep Q, dO (bf16) and the dQ accumulator (fp32) of the group within
     // 64 MiB, about half of L2 (B1 H32 N8192: 16 heads at d = 64, 8 at d = 128).
@@ -878,7 +946,7 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
     a.group = static_cast<int>(std::max(1LL, std::min<long long>(BH, kL2GroupBytes / per_head)));
   }
   const unsigned int grid = static_cast<unsigned int>(a.nkt) * static_cast<unsigned int>(BH);
-  bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_kernel<D, M><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   {
@@ -894,8 +962,12 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
 cudaError_t launch_backward(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, unsigned int* status,
                             unsigned long long timeout_ns, cudaStream_t stream) {
-  if (p.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
-  return launch_bwd_d<128>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
+  if (p.tiles != nullptr) {
+    if (p.d == 64) return launch_bwd_d<64, true>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
+    return launch_bwd_d<128, true>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
+  }
+  if (p.d == 64) return launch_bwd_d<64, false>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
+  return launch_bwd_d<128, false>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
 }
 
 }  // namespace fattn

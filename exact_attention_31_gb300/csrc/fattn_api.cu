@@ -239,7 +239,8 @@ fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, floa
 
 fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, int wl,
-                      int wr, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+                      int wr, float scale, void* workspace, size_t workspace_bytes, void* stream,
+                      const MaskArg& mk = MaskArg()) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
@@ -269,6 +270,16 @@ fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   if (device_status_ptr(&status) != cudaSuccess) return FATTN_ERR_CUDA;
   BwdProblem p{q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, wl, wr, scale, ws_dq, ws_ext_q, ws_ext_do,
                test_drop_bwd_kv()};
+  if (mk.mask != nullptr) {
+    p.mask = mk.mask;
+    p.mask_sb = mk.sb;
+    p.mask_sh = mk.sh;
+    p.mask_words = fattn_mask_row_words(Nk);
+    p.tiles = static_cast<const uint8_t*>(mk.workspace);
+    if (launch_mask_tiles(static_cast<const uint32_t*>(mk.mask), mk.sb, mk.sh, p.mask_words, B, H, Nq, Nk,
+                          static_cast<uint8_t*>(mk.workspace), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return FATTN_ERR_CUDA;
+  }
   if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
@@ -344,6 +355,33 @@ fattn_status fattn_bwd_masked(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes, void* stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, window_left, window_right, scale, workspace,
                   workspace_bytes, stream);
+}
+
+size_t fattn_bwd_mask_workspace_size(int B, int H, int Nq, int Nk, int d) {
+  const size_t a = fattn_bwd_workspace_size(B, H, Nq, d), b = fattn_mask_workspace_size(B, H, Nq, Nk);
+  return a == 0 || b == 0 ? 0 : a + b;
+}
+
+fattn_status fattn_bwd_mask(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                            const void* mask, long long mask_stride_b, long long mask_stride_h, int window_left,
+                            int window_right, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (mask == nullptr || !aligned16(mask) || workspace == nullptr) return FATTN_ERR_INVALID_ARG;
+  if (mask_stride_b < 0 || mask_stride_h < 0 || (mask_stride_b & 3) || (mask_stride_h & 3))
+    return FATTN_ERR_INVALID_ARG;
+  if (!positive_sizes(B, H, Nq, Nk)) return FATTN_ERR_INVALID_ARG;
+  const size_t need = fattn_bwd_mask_workspace_size(B, H, Nq, Nk, d);
+  if (need == 0 || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+  // The backward's own workspace first, the tile summary after it (both multiples of 256 bytes).
+  const size_t bwd_bytes = fattn_bwd_workspace_size(B, H, Nq, d);
+  MaskArg mk;
+  mk.mask = mask;
+  mk.sb = mask_stride_b;
+  mk.sh = mask_stride_h;
+  mk.workspace = static_cast<char*>(workspace) + bwd_bytes;
+  mk.workspace_bytes = workspace_bytes - bwd_bytes;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, window_left, window_right, scale, workspace,
+                  bwd_bytes, stream, mk);
 }
 
 int fattn_decode_num_splits(int B, int H, int Nk, int num_splits) {

@@ -71,6 +71,11 @@ struct BwdProblem {
   // Failure-detection testing only (never set in normal use): the key and value tiles are not
   // loaded, so the kernel's waits for them must give up and report a timeout.
   int drop_kv;
+  // Element mask (null: none), laid out as in FwdProblem, with its tile summary.
+  const void* mask = nullptr;
+  long long mask_sb = 0, mask_sh = 0;
+  int mask_words = 0;
+  const uint8_t* tiles = nullptr;
 };
 
 // Query rows of the backward workspace per head: Nq rounded up to the 128-row query tile.

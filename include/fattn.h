@@ -160,6 +160,24 @@ fattn_status fattn_bwd_masked(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes, void* stream);
 
 /*
+ * fattn_bwd_mask -- fattn_bwd_masked for the element mask of fattn_fwd_mask (same mask, strides, band,
+ * o and lse as that call produced).  Rows with no visible key get dq = 0; keys that no query sees get
+ * dk = dv = 0; query tiles the mask hides from a key tile entirely are skipped for it.
+ *
+ *   workspace  device memory of at least fattn_bwd_mask_workspace_size(B, H, Nq, Nk, d) bytes,
+ *              256-byte aligned, owned by the caller: the backward's workspace
+ *              (fattn_bwd_workspace_size) followed by the mask's tile summary
+ *              (fattn_mask_workspace_size).
+ * Returns FATTN_ERR_INVALID_ARG for a null or misaligned mask, a negative or unaligned stride, or a
+ * short workspace; other arguments as for fattn_bwd_masked.
+ */
+size_t fattn_bwd_mask_workspace_size(int B, int H, int Nq, int Nk, int d);
+fattn_status fattn_bwd_mask(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                            const void* mask, long long mask_stride_b, long long mask_stride_h, int window_left,
+                            int window_right, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fattn_decode_num_splits -- the number of key splits fattn_decode uses for a request.
  *
  * The cached keys are cut into blocks of 64; nblk = ceil(Nk / 64).  `num_splits` = 0 asks for the

@@ -165,3 +165,92 @@ def test_mask_arguments_are_checked(fa):
     assert call(words.data_ptr(), 0, 0, ws.numel() - 1) == 1    # short workspace
     torch.cuda.synchronize()
     assert fa.fattn_mask_row_words(1) == 4 and fa.fattn_mask_row_words(129) == 8 and fa.fattn_mask_row_words(0) == -1
+
+
+# ------------------------------------------------------------------------------------------------
+# Backward under the element mask (fattn_bwd_mask), at the backward's gradient tolerance: each
+# gradient within 1.5e-2 of its own largest magnitude (max) and 5e-3 of its mean magnitude (mean).
+# ------------------------------------------------------------------------------------------------
+GRAD_MAX_REL = 1.5e-2
+GRAD_MEAN_REL = 5e-3
+
+BWD_CASES = [
+    # B, H, Nq, Nk, d, mask kind, density, band
+    (1, 2, 300, 300, 64, "bh", 0.5, (-1, -1)),
+    (2, 2, 257, 400, 128, "b1", 0.3, (-1, -1)),
+    (1, 3, 640, 640, 64, "11", 0.6, (-1, 0)),
+    (1, 2, 513, 513, 128, "bh", 0.8, (-1, 0)),
+    (1, 2, 384, 300, 64, "1h", 0.7, (100, 0)),
+]
+
+
+def _grads_close(grads, refs, what):
+    for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
+        e = np.abs(to64(g) - r)
+        scale_max, scale_mean = np.abs(r).max(), np.abs(r).mean()
+        if scale_max == 0.0:
+            assert e.max() <= 1e-5, (what, name)
+            continue
+        assert e.max() <= GRAD_MAX_REL * scale_max and e.mean() <= GRAD_MEAN_REL * scale_mean, \
+            (what, name, e.max(), scale_max, e.mean(), scale_mean)
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "b{}h{}q{}k{}d{}{}p{}w{}_{}".format(*c[:7], *c[7]))
+def test_masked_backward_matches_oracle(fa, case):
+    from exact_attention_31_gb300.workloads import make_dout
+    B, H, Nq, Nk, d, kind, density, band = case
+    q, k, v = _gen(B, H, Nq, Nk, d, 5700 + Nq + Nk + d)
+    do = make_dout(B, H, Nq, d, 5700 + Nq, device="cuda")
+    mb = _random_mask(_mask_shape(kind, B, H, Nq, Nk), density, 5800 + Nq)
+    mb[..., 7, :] = False  # a row with no visible key (dq = 0 there)
+    words = fa.pack_mask(mb)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fattn_fwd(q, k, v, scale=scale, window=band, mask=words)
+    grads = fa.fattn_bwd(q, k, v, o, lse, do, scale=scale, window=band, mask=words)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    refs = oracle.attention_backward(to64(q), to64(k), to64(v), to64(do), scale=scale, window=band,
+                                     mask=mb.cpu().numpy())
+    _grads_close(grads, refs, str(case))
+    assert torch.all(grads[0][..., 7, :] == 0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_sparse_backward(fa, d):
+    # whole 128 x 128 blocks hidden (skipped by every key tile), a few partial ones, causal band
+    from exact_attention_31_gb300.workloads import make_dout
+    B, H, N = 1, 2, 768
+    q, k, v = _gen(B, H, N, N, d, 5900 + d)
+    do = make_dout(B, H, N, d, 5900 + d, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(5901 + d)
+    blocks = torch.rand((B, H, N // 128, N // 128), generator=g, device="cuda") < 0.5
+    blocks[..., torch.arange(N // 128), torch.arange(N // 128)] = True
+    mb = blocks.repeat_interleave(128, dim=2).repeat_interleave(128, dim=3)
+    partial = torch.rand((B, H, N // 128, N // 128), generator=g, device="cuda") < 0.25
+    noise = torch.rand((B, H, N, N), generator=g, device="cuda") < 0.5
+    mb = torch.where(partial.repeat_interleave(128, dim=2).repeat_interleave(128, dim=3), mb & noise, mb)
+    words = fa.pack_mask(mb)
+    o, lse = fa.fattn_fwd(q, k, v, causal=True, mask=words)
+    grads = fa.fattn_bwd(q, k, v, o, lse, do, causal=True, mask=words)
+    torch.cuda.synchronize()
+    refs = oracle.attention_backward(to64(q), to64(k), to64(v), to64(do), causal=True, mask=mb.cpu().numpy())
+    _grads_close(grads, refs, f"block sparse d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_masked_backward_identities(fa, d):
+    # an all-visible mask and a mask spelling out the causal band give the unmasked backward's dk and
+    # dv bit for bit (the same tiles and arithmetic); dq, accumulated in no fixed order, within rounding
+    from exact_attention_31_gb300.workloads import make_dout
+    B, H, Nq, Nk = 1, 2, 300, 420
+    q, k, v = _gen(B, H, Nq, Nk, d, 6000 + d)
+    do = make_dout(B, H, Nq, d, 6000 + d, device="cuda")
+    i = torch.arange(Nq, device="cuda")[:, None]
+    j = torch.arange(Nk, device="cuda")[None, :]
+    for causal, bits in ((False, torch.ones((Nq, Nk), dtype=torch.bool, device="cuda")), (True, j <= i + (Nk - Nq))):
+        o, lse = fa.fattn_fwd(q, k, v, causal=causal)
+        g0 = fa.fattn_bwd(q, k, v, o, lse, do, causal=causal)
+        g1 = fa.fattn_bwd(q, k, v, o, lse, do, mask=fa.pack_mask(bits))
+        torch.cuda.synchronize()
+        assert torch.equal(g0[1], g1[1]) and torch.equal(g0[2], g1[2]), causal
+        assert (g0[0].float() - g1[0].float()).abs().max().item() <= 2 ** -7 * g0[0].float().abs().max().item()
