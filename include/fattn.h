@@ -253,8 +253,11 @@ fattn_status fattn_decode_masked(const void* q, const void* k_cache, const void*
  *   must not exceed FATTN_DECODE_STATIC_WORKSPACE_BYTES; with num_splits = 0 this only fails when
  *   a single split per (b, h) does not fit).  The other arguments are checked as in fattn_decode.
  *
- * Set-up: the first call on each device looks up the device address of the array, with that
- * device current; make that first call before any stream capture begins.
+ * Set-up: the array is created with the library's device code, which CUDA's lazy module loading
+ * (the default) loads at the first call of any libfattn entry point on a device; that call may
+ * synchronise.  The first call of this entry point on each device also looks up the array's device
+ * address, with that device current.  Make both first calls during set-up, before any stream
+ * capture begins; later calls allocate nothing and do not synchronise.
  * Sharing: every call on a device uses the same array and leaves its contents behind.  No part of
  * it needs clearing: each call writes every partial state it later reads.  Two calls whose work
  * overlaps on the GPU (different streams, or other host threads) race on the array and may return
