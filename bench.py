@@ -541,6 +541,8 @@ def run_ours(args):
         del ws256
     if args.rising and do_prefill and window is None and rank == 0:
         line["prefill_rising_scores"] = measure_rising_scores(fa, dev, stream, P, pre_avg, peaks)
+    if args.configs and do_prefill and window is None and rank == 0:
+        line["prefill_block_sparse_mask"] = measure_block_sparse(fa, dev, stream, P, q, k, v, o, lse, peaks)
     if args.cpu_budget > 0:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if e2e is not None:
@@ -836,6 +838,45 @@ def measure_rising_scores(fa, dev, stream, P, normal_ms, peaks, iters=10):
             "rows_failing_range_check": rows, "rows_total": B * H * N, "ms": round(ms, 4),
             "tflops": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4),
             "time_vs_normal_inputs": round(ms / normal_ms, 3)}
+
+
+def measure_block_sparse(fa, dev, stream, P, q, k, v, o, lse, peaks, iters=10):
+    """The benchmark prefill under an element mask shared by every head: causal, with half of the
+    128 x 128 blocks below the diagonal hidden (seeded), the diagonal blocks visible, and one block in
+    eight with a random pattern inside.  TFLOP/s counts the visible (query, key) pairs only (4 d flops
+    each); the time includes the tile-summary pass.  Outside the benchmark's timed region."""
+    import torch
+    N, d = P["N"], P["d"]
+    T = N // 128
+    g = torch.Generator(device=dev).manual_seed(0xFA77E000 + 8)
+    blocks = torch.rand((T, T), generator=g, device=dev) < 0.5
+    blocks[torch.arange(T), torch.arange(T)] = True
+    partial = torch.rand((T, T), generator=g, device=dev) < 0.125
+    mb = blocks.repeat_interleave(128, 0).repeat_interleave(128, 1)
+    noise = torch.rand((N, N), generator=g, device=dev) < 0.5
+    mb = torch.where(partial.repeat_interleave(128, 0).repeat_interleave(128, 1), mb & noise, mb)
+    mb &= torch.ones((N, N), dtype=torch.bool, device=dev).tril()
+    visible = float(mb.sum().item()) * P["B"] * P["H"]
+    words = fa.pack_mask(mb)
+    del mb, noise
+    ws = torch.empty(fa.fattn_mask_workspace_size(P["B"], P["H"], N, N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale = 1 / math.sqrt(d)
+    for _ in range(3):
+        fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, mask=words, mask_workspace=ws, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, mask=words, mask_workspace=ws, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / iters
+    tf = 4.0 * d * visible / (ms * 1e-3) / 1e12
+    return {"workload": f"prefill_b{P['B']}h{P['H']}_n{N}_d{d} causal, one element mask for all heads: half of "
+                        "the 128x128 blocks below the diagonal hidden, 1 in 8 with random bits inside",
+            "visible_pairs": visible, "ms": round(ms, 4), "tflops_visible": round(tf, 2),
+            "frac": round(tf / peaks["bf16_tflops"], 4)}
 
 
 def run_e2e(fa, dev, stream, args, q, k, v, dq, dk, dv, scale_p, scale_d):

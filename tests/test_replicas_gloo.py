@@ -45,3 +45,24 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.init_dist(1, "gloo") is None
     assert bench.max_over_ranks(3.0, None, "cpu") == 3.0
+
+
+def test_reference_arm_prints_once_under_two_ranks():
+    # `bench.py --impl reference` launched as two ranks: rank 0 times the oracle and prints the one
+    # JSON line, rank 1 exits 0 without work.
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for rank in (0, 1):
+        env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1")
+        p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+                            "--ref-budget", "1"], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+        assert p.returncode == 0, p.stderr[-2000:]
+        outs.append(p.stdout.strip())
+    assert outs[1] == ""
+    line = json.loads(outs[0].splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["gpu_launches"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
