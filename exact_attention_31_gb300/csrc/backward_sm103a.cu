@@ -148,28 +148,40 @@ struct BArgs {
   int nkt;      // key tiles per head
   int group;    // heads per CTA group (1 .. BH)
   // Element mask (masked instantiation only), laid out as for the forward: bit j & 31 of word j >> 5
-  // of query row i of head (b, h) at mask + b * mask_sb + h * mask_sh + i * mask_words, set = visible;
-  // tiles[(bh * tiles_q + i / 128) * tiles_k + j / 128] = 0 (none visible), 1 (some) or 2 (all).
+  // of query row i of head (b, h) at mask + b * mask_sb + h * mask_sh + i * mask_words, set = visible.
+  // Its summary by key tile: for key tile j of head (b, h), at tiles + b * tiles_sb + h * tiles_sh +
+  // j * 2 * tiles_w, tiles_w 64-bit words with bit i & 63 of word i >> 6 set when query tile i sees
+  // a key of the tile, then tiles_w words with the bit set when some of those keys are hidden from it.
   int H;
   const uint32_t* mask;
   long long mask_sb, mask_sh;
   int mask_words;
-  const uint8_t* tiles;
-  int tiles_q;
+  const unsigned long long* tiles;
+  long long tiles_sb, tiles_sh;
+  int tiles_w;
 };
 
-// Under an element mask, the state (0 none, 1 some, 2 all visible) of query tile qt against key tile jt.
-__device__ __forceinline__ int bwd_tile_state(const BArgs& a, int bh, int qt, int jt) {
-  return a.tiles[(static_cast<size_t>(bh) * a.tiles_q + qt) * a.nkt + jt];
+// Under an element mask: the summary words of key tile jt of head bh.
+__device__ __forceinline__ const unsigned long long* key_tile_bits(const BArgs& a, int bh, int jt) {
+  return a.tiles + (bh / a.H) * a.tiles_sb + (bh % a.H) * a.tiles_sh + static_cast<long long>(jt) * 2 * a.tiles_w;
+}
+
+// Under an element mask, whether query tile qt sees some but not all of the key tile's keys.
+__device__ __forceinline__ bool partly_hidden(const BArgs& a, const unsigned long long* bits, int qt) {
+  return (__ldg(bits + a.tiles_w + (qt >> 6)) >> (qt & 63)) & 1ull;
 }
 
 // The query tile after qt (from it0 - 1 on) that this key tile computes: every one without a mask,
-// the ones the mask does not hide entirely with one.
+// the ones the mask does not hide entirely with one (the next set bit of the key tile's live words).
 template <bool M>
-__device__ __forceinline__ int next_qtile(const BArgs& a, int bh, int jt, int qt) {
+__device__ __forceinline__ int next_qtile(const BArgs& a, const unsigned long long* bits, int qt) {
   ++qt;
   if constexpr (M) {
-    while (bwd_tile_state(a, bh, qt, jt) == 0) ++qt;
+    while ((qt >> 6) < a.tiles_w) {
+      const unsigned long long rest = __ldg(bits + (qt >> 6)) >> (qt & 63);
+      if (rest != 0ull) return qt + __ffsll(static_cast<long long>(rest)) - 1;
+      qt = (qt | 63) + 1;
+    }
   }
   return qt;
 }
@@ -237,10 +249,11 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
   const float c = a.c_log2;
   bool ok = true;
   int qt = it0 - 1;  // element mask: the query tile of step i
+  const unsigned long long* bits = M ? key_tile_bits(a, bh, n0 / kBN) : nullptr;
   for (int i = 0; i < n; ++i) {
     const int b = i % C::kSBufs;
     const int dsb = i % C::kDSBufs;
-    if constexpr (M) qt = next_qtile<M>(a, bh, n0 / kBN, qt);
+    if constexpr (M) qt = next_qtile<M>(a, bits, qt);
     if (!warp_wait(sbar + 8 * (C::kSFull + b), (i / C::kSBufs) & 1, ab) ||
         !warp_wait(sbar + 8 * C::kDPFull, i & 1, ab) ||
         (!C::kTwoS && i >= C::kDSBufs && !warp_wait(sbar + 8 * (C::kDSEmpty + dsb), ((i / C::kDSBufs) - 1) & 1, ab))) {
@@ -249,7 +262,7 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
     }
     tc_fence_after();
     const int q0 = (M ? qt : it0 + i) * kBM;
-    const bool partial = M && bwd_tile_state(a, bh, q0 / kBM, n0 / kBN) == 1;  // the same for the whole tile
+    const bool partial = M && partly_hidden(a, bits, qt);  // the same for the whole tile
     const uint32_t tS = tmem + lane_field + C::col_s(b);
     const uint32_t tDP = tmem + lane_field + C::kColDP;
     const uint32_t ds_row = sbase + C::kDSOff + dsb * C::kDSBytes + half * kAtom + kr * 128;
@@ -393,9 +406,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
   int issued = 0;
   bool ok = true;
   int qt = it0 - 1;  // element mask: the query tile of step i
+  const unsigned long long* bits = M ? key_tile_bits(a, bh, n0 / kBN) : nullptr;
   for (int i = 0; i < n && ok; ++i) {
     const int st = i % C::kStages, use = i / C::kStages;
-    if constexpr (M) qt = next_qtile<M>(a, bh, n0 / kBN, qt);
+    if constexpr (M) qt = next_qtile<M>(a, bits, qt);
     const int q0 = (M ? qt : it0 + i) * kBM;
     const size_t r0 = (static_cast<size_t>(bh) * a.Nq_pad + q0) * 16;
 #pragma unroll
@@ -640,9 +654,10 @@ __device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it
   const uint32_t stg = sbase + C::kDQOff;  // two [128 rows][32 fp32] boxes, 128-byte swizzled
   if (issuer) tma_prefetch_desc(tdq);
   int qt = it0 - 1;  // element mask: the query tile of step i
+  const unsigned long long* bits = M ? key_tile_bits(a, bh, n0 / kBN) : nullptr;
   for (int i = 0; i < n; ++i) {
     const int b = i % C::kSBufs;
-    if constexpr (M) qt = next_qtile<M>(a, bh, n0 / kBN, qt);
+    if constexpr (M) qt = next_qtile<M>(a, bits, qt);
     bool fail = !warp_wait(sbar + 8 * (C::kDQFull + b), (i / C::kSBufs) & 1, ab);
     if (!fail) tc_fence_after();
     const int q0 = (M ? qt : it0 + i) * kBM;
@@ -720,8 +735,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   int n = q_lo <= q_hi ? static_cast<int>(q_hi / kBM) + 1 - it0 : 0;
   if constexpr (M) {
     // Only the query tiles the element mask does not hide entirely.
+    const unsigned long long* bits = key_tile_bits(a, bh, jt);
     int live = 0;
-    for (int qt = it0; qt < it0 + n; ++qt) live += bwd_tile_state(a, bh, qt, jt) != 0;
+    for (int wi = it0 >> 6; n > 0 && wi <= (it0 + n - 1) >> 6; ++wi) {
+      const int lo = max(it0 - 64 * wi, 0), hi = min(it0 + n - 64 * wi, 64);
+      const unsigned long long span = (hi == 64 ? ~0ull : (1ull << hi) - 1ull) & (~0ull << lo);
+      live += __popcll(__ldg(bits + wi) & span);
+    }
     n = live;
   }
 
@@ -938,7 +958,8 @@ cudaError_t launch_bwd_d(const BwdProblem& p, const CUtensorMap& tq, const CUten
   a.mask_sh = p.mask_sh;
   a.mask_words = p.mask_words;
   a.tiles = p.tiles;
-  a.tiles_q = (p.Nq + kBM - 1) / kBM;
+  mask_summary_strides(p.mask_sb, p.mask_sh, p.H, p.Nq, p.Nk, true, a.tiles_sb, a.tiles_sh);
+  a.tiles_w = mask_summary_words((p.Nq + kBM - 1) / kBM);
   {
     // Heads per group: as many as keep Q, dO (bf16) and the dQ accumulator (fp32) of the group within
     // 64 MiB, about half of L2 (B1 H32 N8192: 16 heads at d = 64, 8 at d = 128).

@@ -188,9 +188,13 @@ const char* fattn_status_string(int status) {
 namespace fattn {
 namespace {
 
-// Element-mask bytes of the tile summary: one per (head, 128-row query tile, 128-key tile).
+// Bytes of an element mask's tile summary with one slice per head, in the larger of its two layouts
+// (a mask shared over heads or batch entries uses less of it).
 size_t mask_tiles_bytes(int B, int H, int Nq, int Nk) {
-  return align_up(static_cast<size_t>(B) * H * ((Nq + 127) / 128) * ((Nk + 127) / 128), 256);
+  const long long slices = static_cast<long long>(B) * H;
+  const size_t by_query = mask_summary_bytes(slices, Nq, Nk, false);
+  const size_t by_key = mask_summary_bytes(slices, Nq, Nk, true);
+  return align_up(by_query > by_key ? by_query : by_key, 256);
 }
 
 struct MaskArg {
@@ -226,9 +230,10 @@ fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, floa
     p.mask_sb = mk.sb;
     p.mask_sh = mk.sh;
     p.mask_words = fattn_mask_row_words(Nk);
-    p.tiles = static_cast<const uint8_t*>(mk.workspace);
-    if (launch_mask_tiles(static_cast<const uint32_t*>(mk.mask), mk.sb, mk.sh, p.mask_words, B, H, Nq, Nk,
-                          static_cast<uint8_t*>(mk.workspace), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    p.tiles = static_cast<const unsigned long long*>(mk.workspace);
+    if (launch_mask_tiles(static_cast<const uint32_t*>(mk.mask), mk.sb, mk.sh, p.mask_words, B, H, Nq, Nk, false,
+                          static_cast<unsigned long long*>(mk.workspace), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
       return FATTN_ERR_CUDA;
   }
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
@@ -275,9 +280,10 @@ fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     p.mask_sb = mk.sb;
     p.mask_sh = mk.sh;
     p.mask_words = fattn_mask_row_words(Nk);
-    p.tiles = static_cast<const uint8_t*>(mk.workspace);
-    if (launch_mask_tiles(static_cast<const uint32_t*>(mk.mask), mk.sb, mk.sh, p.mask_words, B, H, Nq, Nk,
-                          static_cast<uint8_t*>(mk.workspace), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    p.tiles = static_cast<const unsigned long long*>(mk.workspace);
+    if (launch_mask_tiles(static_cast<const uint32_t*>(mk.mask), mk.sb, mk.sh, p.mask_words, B, H, Nq, Nk, true,
+                          static_cast<unsigned long long*>(mk.workspace), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
       return FATTN_ERR_CUDA;
   }
   if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=

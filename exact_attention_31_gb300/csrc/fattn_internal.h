@@ -31,11 +31,11 @@ struct FwdProblem {
   unsigned long long* recomputed;
   // Element mask (null: none).  Bit j & 31 of word (j >> 5) of row i of head (b, h) at
   // mask + b * mask_sb + h * mask_sh + i * mask_words (32-bit words), set = visible.  `tiles` is its
-  // summary per 128 x 128 tile of each head, as written by launch_mask_tiles.
+  // summary by query tile, as written by launch_mask_tiles.
   const void* mask = nullptr;
   long long mask_sb = 0, mask_sh = 0;
   int mask_words = 0;
-  const uint8_t* tiles = nullptr;
+  const unsigned long long* tiles = nullptr;
 };
 
 struct DecodeProblem {
@@ -71,11 +71,11 @@ struct BwdProblem {
   // Failure-detection testing only (never set in normal use): the key and value tiles are not
   // loaded, so the kernel's waits for them must give up and report a timeout.
   int drop_kv;
-  // Element mask (null: none), laid out as in FwdProblem, with its tile summary.
+  // Element mask (null: none), laid out as in FwdProblem, with its tile summary by key tile.
   const void* mask = nullptr;
   long long mask_sb = 0, mask_sh = 0;
   int mask_words = 0;
-  const uint8_t* tiles = nullptr;
+  const unsigned long long* tiles = nullptr;
 };
 
 // Query rows of the backward workspace per head: Nq rounded up to the 128-row query tile.
@@ -92,11 +92,30 @@ cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUt
 
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
 
-// Element-mask summary: tiles[(bh * ceil(Nq / 128) + i) * ceil(Nk / 128) + j] = 0 when no bit of the
-// 128 x 128 tile (query rows 128 i.., keys 128 j.., inside Nq x Nk) of head bh is set, 2 when all
-// are, 1 otherwise.  Mask layout as in FwdProblem.
+// Element-mask summary.  The mask is judged per 128 x 128 tile (query rows 128 i.., keys 128 j..,
+// inside Nq x Nk) once per slice: one slice per (b, h) the mask's strides tell apart (a zero stride
+// shares a slice), slice (b' * nh + h') with b' = mask_sb ? b : 0, h' = mask_sh ? h : 0 and
+// nh = mask_sh ? H : 1.  Each slice holds, per "major" tile (the query tile i by_key == false, the
+// key tile j when true), `words` 64-bit words of live bits (the tile has a visible key) followed by
+// `words` of partial bits (visible and hidden keys both), bit t & 63 of word t >> 6 for minor tile t
+// (the key tile, or the query tile).  words = ceil(minor tiles / 64).
+__host__ __device__ inline int mask_summary_words(int minor_tiles) { return (minor_tiles + 63) / 64; }
+inline size_t mask_summary_bytes(long long slices, int Nq, int Nk, bool by_key) {
+  const int tq = (Nq + 127) / 128, tk = (Nk + 127) / 128;
+  const int major = by_key ? tk : tq, minor = by_key ? tq : tk;
+  return static_cast<size_t>(slices) * major * 2 * mask_summary_words(minor) * sizeof(unsigned long long);
+}
+// The summary's strides over b and h in 64-bit words (0 where the mask is shared).
+inline void mask_summary_strides(long long mask_sb, long long mask_sh, int H, int Nq, int Nk, bool by_key,
+                                 long long& sb, long long& sh) {
+  const int tq = (Nq + 127) / 128, tk = (Nk + 127) / 128;
+  const long long per_slice =
+      static_cast<long long>(by_key ? tk : tq) * 2 * mask_summary_words(by_key ? tq : tk);
+  sh = mask_sh != 0 ? per_slice : 0;
+  sb = mask_sb != 0 ? (mask_sh != 0 ? H : 1) * per_slice : 0;
+}
 cudaError_t launch_mask_tiles(const uint32_t* mask, long long mask_sb, long long mask_sh, int mask_words, int B,
-                              int H, int Nq, int Nk, uint8_t* tiles, cudaStream_t stream);
+                              int H, int Nq, int Nk, bool by_key, unsigned long long* tiles, cudaStream_t stream);
 
 // Backward: q, k, v, dout as for the prefill; tdq describes ws_dq as a 3-D [B*H][Nq_pad][d] fp32
 // tensor with 32-element (128-byte) inner boxes of 128 rows and 128-byte swizzle.

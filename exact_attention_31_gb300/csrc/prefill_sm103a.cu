@@ -125,13 +125,16 @@ struct Args {
   unsigned long long timeout_ns;
   int drop_kv_block;  // failure-detection testing only; -1 = off
   // Element mask (masked instantiation only): bit j & 31 of word (j >> 5) of row i of head (b, h) at
-  // mask + b * mask_sb + h * mask_sh + i * mask_words, set = visible; tiles[(bh * tiles_q + i / 128)
-  // * tiles_k + j / 128] = 0 when no bit of that 128 x 128 tile is set, 1 when some are, 2 when all are.
+  // mask + b * mask_sb + h * mask_sh + i * mask_words, set = visible.  Its summary by query tile: for
+  // query tile i of head (b, h), at tiles + b * tiles_sb + h * tiles_sh + i * 2 * tiles_w, tiles_w
+  // 64-bit words with bit j & 63 of word j >> 6 set when key tile j holds a visible key of the tile,
+  // then tiles_w words with the bit set when it holds hidden ones too.
   const uint32_t* mask;
   long long mask_sb, mask_sh;
   int mask_words;
-  const uint8_t* tiles;
-  int tiles_q, tiles_k;
+  const unsigned long long* tiles;
+  long long tiles_sb, tiles_sh;
+  int tiles_w;
 };
 
 // Key/value tiles [jb, je) that query tile [r0, r0 + 128) must visit: those holding a key visible to
@@ -170,29 +173,57 @@ struct Unit {
   int jb[2], je[2];
 };
 
-// The k-th unit of this CTA.  The grid is persistent (at most one CTA per SM); units are taken in
-// rounds of gridDim.x, heaviest causal units (last query rows) first, and every other round is
-// walked backwards so that each CTA's total is closer to the others'.  Returns false past the end.
-// Under an element mask, 0 (no visible key), 1 (some) or 2 (all) for key tile j of query tile t.
-__device__ __forceinline__ int tile_state(const Args& a, const Unit& u, int t, int j) {
-  return a.tiles[(static_cast<size_t>(u.bh) * a.tiles_q + (u.row0 / kBlockM + t)) * a.tiles_k + j];
+// Under an element mask: the summary words of query tile qt of head bh.
+__device__ __forceinline__ const unsigned long long* tile_bits(const Args& a, int bh, int qt) {
+  return a.tiles + (bh / a.H) * a.tiles_sb + (bh % a.H) * a.tiles_sh + static_cast<long long>(qt) * 2 * a.tiles_w;
+}
+
+// Bits of tiles [b, e) among the 64 from 64 wi on.
+__device__ __forceinline__ unsigned long long span_bits(int b, int e, int wi) {
+  const int lo = max(b - 64 * wi, 0), hi = min(e - 64 * wi, 64);
+  if (lo >= hi) return 0ull;
+  return (hi == 64 ? ~0ull : (1ull << hi) - 1ull) & (~0ull << lo);
+}
+
+// Under an element mask, the key tiles [64 wi, 64 wi + 64) each query tile of a unit computes: its
+// summary word cut to its key range, loaded as a walk over the range reaches a new word.  Scalars,
+// not an array, so that a warp whose tile index is a run-time value keeps them in registers.
+struct LiveWords {
+  int wi = -1;
+  unsigned long long w0 = 0ull, w1 = 0ull;
+};
+
+__device__ __forceinline__ void live_words(const Args& a, const Unit& u, LiveWords& lw, int wi) {
+  if (lw.wi == wi) return;
+  lw.wi = wi;
+  const int qt = u.row0 / kBlockM;
+  lw.w0 = u.je[0] > u.jb[0] ? __ldg(tile_bits(a, u.bh, qt) + wi) & span_bits(u.jb[0], u.je[0], wi) : 0ull;
+  lw.w1 = u.je[1] > u.jb[1] ? __ldg(tile_bits(a, u.bh, qt + 1) + wi) & span_bits(u.jb[1], u.je[1], wi) : 0ull;
 }
 
 // Whether query tile t of the unit computes key tile j: inside its range and, under an element mask,
 // not a tile the mask leaves empty.
 template <bool M>
-__device__ __forceinline__ bool live(const Args& a, const Unit& u, int t, int j) {
-  if (!(u.jb[t] <= j && j < u.je[t])) return false;
-  if constexpr (M) return tile_state(a, u, t, j) != 0;
-  return true;
+__device__ __forceinline__ bool live(const Args& a, const Unit& u, LiveWords& lw, int t, int j) {
+  if constexpr (M) {
+    live_words(a, u, lw, j >> 6);
+    return ((t ? lw.w1 : lw.w0) >> (j & 63)) & 1ull;
+  }
+  return t ? (u.jb[1] <= j && j < u.je[1]) : (u.jb[0] <= j && j < u.je[0]);
 }
 
 // The key tile after j that either query tile of the unit computes (J1 when none is left).
 template <bool M>
-__device__ __forceinline__ int next_live(const Args& a, const Unit& u, int j, int J1) {
+__device__ __forceinline__ int next_live(const Args& a, const Unit& u, LiveWords& lw, int j, int J1) {
   ++j;
   if constexpr (M) {
-    while (j < J1 && !live<M>(a, u, 0, j) && !live<M>(a, u, 1, j)) ++j;
+    while (j < J1) {
+      live_words(a, u, lw, j >> 6);
+      const unsigned long long rest = (lw.w0 | lw.w1) >> (j & 63);
+      if (rest != 0ull) return j + __ffsll(static_cast<long long>(rest)) - 1;
+      j = (j | 63) + 1;
+    }
+    return J1;
   }
   return j;
 }
@@ -201,13 +232,19 @@ __device__ __forceinline__ int next_live(const Args& a, const Unit& u, int j, in
 template <bool M>
 __device__ __forceinline__ int live_count(const Args& a, const Unit& u, int t) {
   if constexpr (M) {
+    if (u.je[t] <= u.jb[t]) return 0;
+    const unsigned long long* bits = tile_bits(a, u.bh, u.row0 / kBlockM + t);
     int n = 0;
-    for (int j = u.jb[t]; j < u.je[t]; ++j) n += tile_state(a, u, t, j) != 0;
+    for (int wi = u.jb[t] >> 6; wi <= (u.je[t] - 1) >> 6; ++wi)
+      n += __popcll(__ldg(bits + wi) & span_bits(u.jb[t], u.je[t], wi));
     return n;
   }
   return u.je[t] - u.jb[t];
 }
 
+// The k-th unit of this CTA.  The grid is persistent (at most one CTA per SM); units are taken in
+// rounds of gridDim.x, heaviest causal units (last query rows) first, and every other round is
+// walked backwards so that each CTA's total is closer to the others'.  Returns false past the end.
 template <bool M>
 __device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
@@ -223,11 +260,17 @@ __device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
     // is empty (its rows get o = 0 and L = -inf).
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-      int b = u.jb[t], e = u.je[t];
-      while (b < e && tile_state(a, u, t, b) == 0) ++b;
-      while (e > b && tile_state(a, u, t, e - 1) == 0) --e;
-      u.jb[t] = b < e ? b : 0;
-      u.je[t] = b < e ? e : 0;
+      if (u.je[t] <= u.jb[t]) continue;
+      const unsigned long long* bits = tile_bits(a, u.bh, u.row0 / kBlockM + t);
+      int b = -1, e = 0;
+      for (int wi = u.jb[t] >> 6; wi <= (u.je[t] - 1) >> 6; ++wi) {
+        const unsigned long long w = __ldg(bits + wi) & span_bits(u.jb[t], u.je[t], wi);
+        if (w == 0ull) continue;
+        if (b < 0) b = 64 * wi + __ffsll(static_cast<long long>(w)) - 1;
+        e = 64 * wi + 64 - __clzll(static_cast<long long>(w));
+      }
+      u.jb[t] = b >= 0 ? b : 0;
+      u.je[t] = b >= 0 ? e : 0;
     }
   }
   return true;
@@ -329,6 +372,13 @@ __device__ __noinline__ void mark_row(const Args& a, uint32_t sbar, int k, int t
   atomicAdd(a.recomputed, 1ull);
 }
 
+// Bits i of a 32-bit word with lo <= i <= hi (either bound may lie outside [0, 31]).
+__device__ __forceinline__ uint32_t bits_between(int lo, int hi) {
+  const int l = max(lo, 0), h = min(hi, 31);
+  if (l > h) return 0u;
+  return (0xffffffffu >> (31 - h)) & (0xffffffffu << l);
+}
+
 // Max of a row's 128 scores in eight independent chains of three-input maxes: fewer live temporaries
 // than the tree below (the redo phase takes it at every step, with all 128 scores live).
 __device__ __forceinline__ float max128_chains(const uint32_t (&s)[4][32]) {
@@ -399,22 +449,26 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
   float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled score
   float l = 0.f;            // sum of the fp32 weights: O = O / l, L = m + log(l)
   bool ok = true;
-  // Element mask: this tile's row of tile states and this row's mask words (rows past Nq read none).
-  const uint8_t* states = nullptr;
-  const uint32_t* mrow = nullptr;
+  // Element mask: this tile's summary words and this row's mask words (rows past Nq read none).  The
+  // walk visits the key tiles whose live bit is set; a tile's partial bit (the same for the whole
+  // tile) says whether the row's 128 bits for it are needed.
+  const unsigned long long* bits = nullptr;
+  const uint4* mrow = nullptr;
   if constexpr (M) {
-    states = a.tiles + (static_cast<size_t>(bh) * a.tiles_q + row0 / kBlockM + t) * a.tiles_k;
+    bits = tile_bits(a, bh, row0 / kBlockM + t);
     if (q_row < a.Nq)
-      mrow = a.mask + (bh / a.H) * a.mask_sb + (bh % a.H) * a.mask_sh + static_cast<long long>(q_row) * a.mask_words;
+      mrow = reinterpret_cast<const uint4*>(a.mask + (bh / a.H) * a.mask_sb + (bh % a.H) * a.mask_sh +
+                                            static_cast<long long>(q_row) * a.mask_words);
   }
   int jm = jb;  // element mask: the key tile of this step (the tiles the mask leaves empty are skipped)
   for (int step = 0; step < n_tiles; ++step, ++g) {
     const int j = M ? jm : jb + step;
     uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);  // the row's 128 mask bits for key tile j
     bool partial = false;
+    unsigned long long live_w = 0ull, part_w = 0ull;
     if constexpr (M) {
-      partial = states[j] == 1;  // the same for the whole tile
-      if (partial && mrow != nullptr) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + j);
+      live_w = __ldg(bits + (j >> 6));
+      part_w = __ldg(bits + a.tiles_w + (j >> 6));
     }
     if (!warp_wait(sbar + 8 * (C::kSFull + t), g & 1, ab)) {
       ok = false;
@@ -434,46 +488,50 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
     }
 
     const int kv0 = j * kBlockN;
-    if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > hi || kv0 < lo)) {
-      // Keys outside this row's visible range, as offsets into the tile: one compare with an
-      // immediate per key and side, and only the sides that cut into this tile for some row of the
-      // warp (a causal diagonal tile or a band's upper edge: the upper side; a band's lower edge:
-      // the lower side).
-      const int vhi = hi - kv0, vlo = lo - kv0;
-      const bool cut_lo = __any_sync(0xffffffffu, vlo > 0);
-      const bool cut_hi = __any_sync(0xffffffffu, vhi < kBlockN - 1);
-      if (!cut_lo) {
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * h + i > vhi) s[h][i] = __float_as_uint(-INFINITY);
-      } else if (!cut_hi) {
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
-      } else {
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
-      }
-    }
     if constexpr (M) {
-      if (partial) {
-        const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
+      // Band and element mask in one pass: bit i of vis[h] says whether key kv0 + 32 h + i is
+      // visible to this row; only tiles the band cuts or the mask partly hides take it.
+      const bool cut = __any_sync(0xffffffffu, kv0 + kBlockN - 1 > hi || kv0 < lo);
+      partial = (part_w >> (j & 63)) & 1ull;
+      if (partial && mrow != nullptr) mw = __ldg(mrow + j);
+      if (cut || partial) {
+        uint32_t vis[4] = {mw.x, mw.y, mw.z, mw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) vis[h] &= bits_between(lo - kv0 - 32 * h, hi - kv0 - 32 * h);
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (!((words[h] >> i) & 1u)) s[h][i] = __float_as_uint(-INFINITY);
+            if (!((vis[h] >> i) & 1u)) s[h][i] = __float_as_uint(-INFINITY);
       }
-      if (step + 1 < n_tiles) {
-        do ++jm;
-        while (states[jm] == 0);
+    } else {
+      if (__any_sync(0xffffffffu, kv0 + kBlockN - 1 > hi || kv0 < lo)) {
+        // Keys outside this row's visible range, as offsets into the tile: one compare with an
+        // immediate per key and side, and only the sides that cut into this tile for some row of the
+        // warp (a causal diagonal tile or a band's upper edge: the upper side; a band's lower edge:
+        // the lower side).
+        const int vhi = hi - kv0, vlo = lo - kv0;
+        const bool cut_lo = __any_sync(0xffffffffu, vlo > 0);
+        const bool cut_hi = __any_sync(0xffffffffu, vhi < kBlockN - 1);
+        if (!cut_lo) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * h + i > vhi) s[h][i] = __float_as_uint(-INFINITY);
+        } else if (!cut_hi) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * h + i > vhi || 32 * h + i < vlo) s[h][i] = __float_as_uint(-INFINITY);
+        }
       }
     }
     float corr = 1.f;  // redo phase: factor for l and O when the reference moved in this step
@@ -552,6 +610,23 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
     if (lane == 0) mbar_arrive(sbar + 8 * (C::kPFull + t));
     // The row sum is not needed by the hand-off: P_t goes to the MMA warp first.
     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    if constexpr (M) {
+      if (step + 1 < n_tiles) {
+        // The next live tile: in j's word or a later one.
+        const unsigned long long rest = (live_w >> (j & 63)) >> 1;
+        if (rest != 0ull) {
+          jm = j + __ffsll(static_cast<long long>(rest));
+        } else {
+          for (int w = (j >> 6) + 1; w < a.tiles_w; ++w) {
+            const unsigned long long x = __ldg(bits + w);
+            if (x != 0ull) {
+              jm = 64 * w + __ffsll(static_cast<long long>(x)) - 1;
+              break;
+            }
+          }
+        }
+      }
+    }
   }
   if (!ok) return false;
   const bool store = q_row < a.Nq;
@@ -690,7 +765,8 @@ __device__ __forceinline__ bool producer_unit(const Unit& u, const CUtensorMap* 
   }
   const int J0 = union_begin(u.jb, u.je), J1 = union_end(u.jb, u.je);
   int n = 0;  // key tiles loaded for this unit (ring index ring + 2 n + w)
-  for (int j = J0; j < J1; j = next_live<M>(a, u, j, J1), ++n) {
+  LiveWords lw;
+  for (int j = J0; j < J1; j = next_live<M>(a, u, lw, j, J1), ++n) {
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
       const int idx = ps.ring + 2 * n + w;
@@ -894,22 +970,23 @@ __device__ __forceinline__ bool mma_unit_tile(int t, const Unit& u, const MmaCtx
   const int r0 = st.ring;
   if constexpr (M) {
     // The same schedule over the key tiles either query tile computes (n-th loaded: ring r0 + 2 n).
+    LiveWords lw;
     if (!m.wait_kv(r0, ab)) return false;
     tc_fence_after();
-    if (live<M>(a, u, t, J0) && !issue_s_step<D>(t, r0 % C::kSlots, J0 == je - 1, m, st, ab)) return false;
+    if (live<M>(a, u, lw, t, J0) && !issue_s_step<D>(t, r0 % C::kSlots, J0 == je - 1, m, st, ab)) return false;
     m.commit(C::kKVEmpty + r0 % C::kSlots);
     int n = 0;
     for (int j = J0; j < J1; ++n) {
-      const int jn = next_live<M>(a, u, j, J1);
+      const int jn = next_live<M>(a, u, lw, j, J1);
       if (jn < J1) {
         const int kidx = r0 + 2 * (n + 1);
         if (!m.wait_kv(kidx, ab)) return false;
-        if (live<M>(a, u, t, jn) && !issue_s_step<D>(t, kidx % C::kSlots, jn == je - 1, m, st, ab)) return false;
+        if (live<M>(a, u, lw, t, jn) && !issue_s_step<D>(t, kidx % C::kSlots, jn == je - 1, m, st, ab)) return false;
         m.commit(C::kKVEmpty + kidx % C::kSlots);
       }
       const int vidx = r0 + 2 * n + 1;
       if (!m.wait_kv(vidx, ab)) return false;
-      if (live<M>(a, u, t, j) && !issue_pv_step<D>(t, vidx % C::kSlots, j == jb, j == je - 1, m, st, ab)) return false;
+      if (live<M>(a, u, lw, t, j) && !issue_pv_step<D>(t, vidx % C::kSlots, j == jb, j == je - 1, m, st, ab)) return false;
       m.commit(C::kKVEmpty + vidx % C::kSlots);
       j = jn;
     }
@@ -951,6 +1028,7 @@ __device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D
     // The same schedule over the key tiles either query tile computes: the n-th loaded tile j (ring
     // r0 + 2 n) after the previous one jp.
     int j = J0, jp = -1, n = 0;
+    LiveWords lw;
     for (;;) {
       const int r = r0 + 2 * n;
       if (j < J1 && !m.wait_kv(r, ab)) return false;
@@ -958,17 +1036,17 @@ __device__ __forceinline__ bool mma_unit_aliased_p(const Unit& u, const MmaCtx<D
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
-        if (n > 0 && live<M>(a, u, t, jp) &&
+        if (n > 0 && live<M>(a, u, lw, t, jp) &&
             !issue_pv_step<D>(t, (r - 1) % C::kSlots, jp == u.jb[t], jp == u.je[t] - 1, m, st, ab))
           return false;
-        if (j < J1 && live<M>(a, u, t, j) && !issue_s_step<D>(t, r % C::kSlots, j == u.je[t] - 1, m, st, ab))
+        if (j < J1 && live<M>(a, u, lw, t, j) && !issue_s_step<D>(t, r % C::kSlots, j == u.je[t] - 1, m, st, ab))
           return false;
       }
       if (j < J1) m.commit(C::kKVEmpty + r % C::kSlots);
       if (n > 0) m.commit(C::kKVEmpty + (r - 1) % C::kSlots);
       if (j >= J1) break;
       jp = j;
-      j = next_live<M>(a, u, j, J1);
+      j = next_live<M>(a, u, lw, j, J1);
       ++n;
     }
     st.ring = r0 + 2 * n;
@@ -1154,8 +1232,8 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   a.mask_sh = p.mask_sh;
   a.mask_words = p.mask_words;
   a.tiles = p.tiles;
-  a.tiles_q = (p.Nq + kBlockM - 1) / kBlockM;
-  a.tiles_k = (p.Nk + kBlockN - 1) / kBlockN;
+  mask_summary_strides(p.mask_sb, p.mask_sh, p.H, p.Nq, p.Nk, false, a.tiles_sb, a.tiles_sh);
+  a.tiles_w = mask_summary_words((p.Nk + kBlockN - 1) / kBlockN);
   // Persistent: one CTA per SM (each holds all of an SM's tensor memory), looping over the units.
   static int sm_count[64] = {};
   if (dev < 0 || dev >= 64 || sm_count[dev] == 0) {

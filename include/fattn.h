@@ -101,10 +101,11 @@ fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void*
  *             that dimension (one mask for every head: mask_stride_h = 0).
  *   window_left, window_right   the band of fattn_fwd_masked ((-1, -1) for the element mask alone).
  *   workspace device memory of at least fattn_mask_workspace_size(B, H, Nq, Nk) bytes, owned by the
- *             caller: it receives one byte per (head, 128-query tile, 128-key tile) telling whether the
- *             mask hides all, some or none of that tile.  Tiles it hides entirely are skipped (no
- *             loads, no products); only partly hidden tiles read the mask bits.  Calls sharing a
- *             workspace must not overlap.
+ *             caller: it receives the mask's tile summary, two bits per 128-query by 128-key tile
+ *             telling whether the mask hides all, some or none of it, written once per distinct
+ *             mask (once in all for mask_stride_b = mask_stride_h = 0).  Tiles it hides entirely are
+ *             skipped (no loads, no products); only partly hidden tiles read the mask bits.  Calls
+ *             sharing a workspace must not overlap.
  *
  * A row with no visible key gets o = 0 and L = -inf.  Two kernels run on `stream`: the tile summary,
  * then the forward.  Returns FATTN_ERR_INVALID_ARG for a null or misaligned mask, a negative or

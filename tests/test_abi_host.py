@@ -221,12 +221,20 @@ def test_decode_host_rejects_bad_arguments(L, change, expect):
 
 
 def test_mask_row_words_and_workspace(L):
-    # four 32-bit words per 128 keys, so every mask row starts on 16 bytes; one summary byte per
-    # (head, 128-query tile, 128-key tile), padded to 256 bytes
+    # four 32-bit words per 128 keys, so every mask row starts on 16 bytes; the summary holds, per
+    # head and per 128-row query tile (forward) or 128-key tile (backward), two sets of bits over the
+    # other kind of tile in 64-bit words: the larger layout, padded to 256 bytes
     assert L.fattn_mask_row_words(1) == 4 and L.fattn_mask_row_words(128) == 4 and L.fattn_mask_row_words(129) == 8
     assert L.fattn_mask_row_words(0) == -1
-    assert L.fattn_mask_workspace_size(2, 3, 300, 1000) == (2 * 3 * 3 * 8 + 255) // 256 * 256
-    assert L.fattn_mask_workspace_size(1, 32, 8192, 8192) == 32 * 64 * 64
+
+    def summary(B, H, Nq, Nk):
+        tq, tk = -(-Nq // 128), -(-Nk // 128)
+        per_head = max(tq * 2 * -(-tk // 64), tk * 2 * -(-tq // 64)) * 8
+        return -(-B * H * per_head // 256) * 256
+
+    assert L.fattn_mask_workspace_size(2, 3, 300, 1000) == summary(2, 3, 300, 1000) == 768
+    assert L.fattn_mask_workspace_size(1, 32, 8192, 8192) == summary(1, 32, 8192, 8192) == 32 * 64 * 16
+    assert L.fattn_mask_workspace_size(1, 1, 128, 65536) == summary(1, 1, 128, 65536) == 512 * 16
     assert L.fattn_mask_workspace_size(1, 1, 0, 8) == 0
 
 
