@@ -79,7 +79,7 @@ template <int D>
 struct BCfg {
   static constexpr bool kTwoS = (D == 64);
   static constexpr int kSBufs = kTwoS ? 2 : 1;
-  static constexpr int kStages = kTwoS ? 3 : 1;   // Q_i/dO_i buffers
+  static constexpr int kStages = kTwoS ? 2 : 1;   // Q_i/dO_i buffers (d = 64: two measured 2 % faster than three)
   static constexpr int kDSBufs = 1;               // dS^T buffers
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kTile = kBM * D * 2;  // one 128-row bf16 tile of Q, K, V or dO
