@@ -6,6 +6,10 @@ backward, and a split-KV decode kernel with its combine kernel) behind the C ABI
 module only marshals torch tensors into that ABI: it checks dtypes, devices and shapes, allocates
 outputs with torch when the caller does not pass them, and raises on a non-OK status.  There is no
 other implementation behind these names: if the library is missing, every call raises.
+
+With FATTN_DEBUG=1 in the environment when this module is imported, the same calls go to
+``libfattn_debug.so``, the build whose kernels check their TMA, tensor-memory and barrier operands
+and their output stores on the device (``fattn_debug_take`` reads what they found).
 """
 
 from __future__ import annotations
@@ -33,17 +37,22 @@ __all__ = [
     "fattn_fwd_recomputed_rows",
     "fattn_last_error",
     "fattn_status_string",
+    "fattn_debug_build",
+    "fattn_debug_take",
     "lib",
     "LIB_PATH",
 ]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn.so")
+RELEASE_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn.so")
+DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn_debug.so")
+LIB_PATH = DEBUG_LIB_PATH if os.environ.get("FATTN_DEBUG") == "1" else RELEASE_LIB_PATH
 
 FATTN_OK = 0
 FATTN_ERR_INVALID_ARG = 1
 FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
+FATTN_ERR_DEBUG = 5
 
 _lib = None
 
@@ -66,6 +75,10 @@ def lib() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     L.fattn_fwd.restype = i
+    L.fattn_debug_build.argtypes = []
+    L.fattn_debug_build.restype = i
+    L.fattn_debug_take.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_ulonglong)]
+    L.fattn_debug_take.restype = i
     L.fattn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.fattn_fwd_masked.restype = i
     ll = ctypes.c_longlong
@@ -551,6 +564,23 @@ def fattn_fwd_recomputed_rows() -> int:
 
 
 def fattn_last_error(stream=None) -> int:
-    """Synchronise ``stream`` and read-and-clear the on-device status word (0 = OK, 4 = timeout)."""
+    """Synchronise ``stream`` and read-and-clear the on-device status word (0 = OK, 4 = timeout;
+    5 = a device-side check failed, debug builds only)."""
     import torch
     return lib().fattn_last_error(_stream_handle(stream, torch.device("cuda", torch.cuda.current_device())))
+
+
+def fattn_debug_build() -> bool:
+    """True when the loaded library is the build with device-side checks."""
+    return bool(lib().fattn_debug_build())
+
+
+def fattn_debug_take() -> tuple[int, int]:
+    """(rules, first) of the device-side checks since the last call, then cleared (fattn_debug_take):
+    rules is the OR of the broken rules' bits, first the first failure as block << 32 | thread << 8 |
+    rule index + 1.  (0, 0) in release builds."""
+    rules, first = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+    st = lib().fattn_debug_take(ctypes.byref(rules), ctypes.byref(first))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_debug_take")
+    return int(rules.value), int(first.value)

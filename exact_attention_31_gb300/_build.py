@@ -1,7 +1,9 @@
 """Build libfattn.so in-tree with nvcc for sm_103a (no cmake, no torch extension machinery).
 
 The translation units are compiled in parallel and linked into one shared library that
-exports the C ABI declared in include/fattn.h.
+exports the C ABI declared in include/fattn.h.  The same sources built with -DFATTN_DEBUG give
+libfattn_debug.so, whose kernels check every TMA, tensor-memory and barrier operand and every output
+store before they issue it (fattn.h, "Debug builds"); both are built together.
 """
 
 from __future__ import annotations
@@ -20,6 +22,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 STAMP = os.path.join(BUILD, "libfattn.stamp")
+DEBUG_BUILD = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libfattn_debug.so")
+DEBUG_STAMP = os.path.join(DEBUG_BUILD, "libfattn_debug.stamp")
+DEBUG_FLAGS = ["-DFATTN_DEBUG"]
 
 SOURCES = ["fattn_api.cu", "prefill_sm103a.cu", "prefill_fp8_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu",
            "host_staging.cu", "mask_tiles_sm103a.cu"]
@@ -58,29 +64,44 @@ def source_digest(extra_flags=None) -> str:
     return h.hexdigest()
 
 
-def up_to_date(extra_flags=None) -> bool:
-    """True when libfattn.so exists and was built here from exactly the current sources."""
-    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+def _paths(debug: bool):
+    return (DEBUG_BUILD, DEBUG_LIB, DEBUG_STAMP) if debug else (BUILD, LIB, STAMP)
+
+
+def _flags(debug: bool, extra_flags=None):
+    return (DEBUG_FLAGS if debug else []) + list(extra_flags or [])
+
+
+def up_to_date(extra_flags=None, debug: bool = False) -> bool:
+    """True when the library exists and was built here from exactly the current sources."""
+    _, lib, stamp = _paths(debug)
+    if not os.path.exists(lib) or not os.path.exists(stamp):
         return False
-    with open(STAMP) as f:
-        return f.read().strip() == source_digest(extra_flags)
+    with open(stamp) as f:
+        return f.read().strip() == source_digest(_flags(debug, extra_flags))
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date(extra_flags):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def _start(debug: bool, extra_flags, verbose: bool):
+    """Start the nvcc processes of one variant; returns what _finish needs."""
+    build_dir, _, _ = _paths(debug)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + _flags(debug, extra_flags)
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    return debug, extra_flags, procs, objs
+
+
+def _finish(job, verbose: bool) -> str:
+    debug, extra_flags, procs, objs = job
+    _, lib, stamp = _paths(debug)
     failed = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -89,16 +110,30 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         if p.returncode != 0:
             failed.append(src)
     if failed:
-        raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
-        f.write(source_digest(extra_flags) + "\n")
-    return LIB
+        raise RuntimeError(f"nvcc failed for {failed}" + (" (debug build)" if debug else ""))
+    tmp = lib + f".tmp{os.getpid()}"
+    subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
+        f.write(source_digest(_flags(debug, extra_flags)) + "\n")
+    return lib
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    """Build one variant (the release library, or with debug=True the checked one)."""
+    if not force and up_to_date(extra_flags, debug):
+        return _paths(debug)[1]
+    return _finish(_start(debug, extra_flags, verbose), verbose)
+
+
+def build_all(force: bool = False, verbose: bool = False) -> None:
+    """Build the release and debug libraries, all translation units compiled at once."""
+    jobs = [_start(d, None, verbose) for d in (False, True) if force or not up_to_date(None, d)]
+    for job in jobs:
+        _finish(job, verbose)
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    build_all(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(LIB)
+    print(DEBUG_LIB)

@@ -355,7 +355,8 @@ __device__ __forceinline__ void compute_role(int n, int it0, int n0, int bh, uin
   // Epilogue: dV and scale * dK rows of this warp's keys, this warp's half of the columns.
   if (!warp_wait(sbar + 8 * C::kAccDone, 0, ab)) return;
   tc_fence_after();
-  const bool store = kidx < a.Nk;
+  const bool store =
+      kidx < a.Nk && dbg_in(static_cast<long long>(bh) * a.Nk + kidx, static_cast<long long>(a.BH) * a.Nk);
   const size_t row = (static_cast<size_t>(bh) * a.Nk + (store ? kidx : 0)) * D;
 #pragma unroll
   for (int w = 0; w < 2; ++w) {
@@ -871,7 +872,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 #pragma unroll
   for (int s = G / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (!live) return;
+  if (!live || !dbg_in(bh * Nq_pad + i, static_cast<long long>(BH) * Nq_pad)) return;
   float4* z = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * Nq_pad + i) * D + 8 * g);
   z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
   z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -895,6 +896,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
   const int g = static_cast<int>(t % (D / 8));
   const long long bh = r / Nq;
   const int i = static_cast<int>(r % Nq);
+  if (!dbg_in(r, static_cast<long long>(BH) * Nq)) return;
   const float4* src = reinterpret_cast<const float4*>(dq_acc + (static_cast<size_t>(bh) * Nq_pad + i) * D + 8 * g);
   const float4 x = src[0], y = src[1];
   uint4 out;
@@ -990,5 +992,8 @@ cudaError_t launch_backward(const BwdProblem& p, const CUtensorMap& tq, const CU
   if (p.d == 64) return launch_bwd_d<64, false>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
   return launch_bwd_d<128, false>(p, tq, tk, tv, tdo, tdq, status, timeout_ns, stream);
 }
+
+// Debug builds: read (and optionally clear) this file's device-side check record.
+FATTN_DEBUG_ACCESSOR(backward)
 
 }  // namespace fattn

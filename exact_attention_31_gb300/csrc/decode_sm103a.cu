@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     m = mm;
   }
   const size_t part = static_cast<size_t>(bh) * S + s;
+  if (!dbg_in(static_cast<long long>(part), static_cast<long long>(BH) * S)) return;
   if (sub == 0) {
     float4* dst = reinterpret_cast<float4*>(ws_o + part * D + chunk * 8);
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -253,5 +254,8 @@ cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream) {
   if (p.d == 64) return launch_decode_d<64>(p, stream);
   return launch_decode_d<128>(p, stream);
 }
+
+// Debug builds: read (and optionally clear) this file's device-side check record.
+FATTN_DEBUG_ACCESSOR(decode)
 
 }  // namespace fattn

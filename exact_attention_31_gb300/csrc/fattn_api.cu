@@ -179,6 +179,7 @@ const char* fattn_status_string(int status) {
     case FATTN_ERR_UNSUPPORTED: return "FATTN_ERR_UNSUPPORTED";
     case FATTN_ERR_CUDA: return "FATTN_ERR_CUDA";
     case FATTN_ERR_TIMEOUT: return "FATTN_ERR_TIMEOUT";
+    case FATTN_ERR_DEBUG: return "FATTN_ERR_DEBUG";
     default: return "FATTN_UNKNOWN_STATUS";
   }
 }
@@ -186,6 +187,37 @@ const char* fattn_status_string(int status) {
 }  // extern "C"
 
 namespace fattn {
+
+cudaError_t debug_collect(unsigned int* rules, unsigned long long* first, bool clear) {
+  cudaError_t (*const parts[])(unsigned int*, unsigned long long*, bool) = {debug_take_prefill, debug_take_fp8,
+                                                                            debug_take_backward, debug_take_decode};
+  *rules = 0u;
+  *first = 0ull;
+  for (auto take : parts) {
+    unsigned int r = 0u;
+    unsigned long long f = 0ull;
+    const cudaError_t e = take(&r, &f, clear);
+    if (e != cudaSuccess) return e;
+    *rules |= r;
+    if (*first == 0ull) *first = f;
+  }
+  return cudaSuccess;
+}
+
+fattn_status debug_after(void* stream, fattn_status s) {
+#ifdef FATTN_DEBUG
+  if (s != FATTN_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  unsigned int rules = 0u;
+  unsigned long long first = 0ull;
+  if (debug_collect(&rules, &first, false) != cudaSuccess) return FATTN_ERR_CUDA;
+  return rules != 0u ? FATTN_ERR_DEBUG : FATTN_OK;
+#else
+  (void)stream;
+  return s;
+#endif
+}
+
 namespace {
 
 // Bytes of an element mask's tile summary with one slice per head, in the larger of its two layouts
@@ -239,7 +271,7 @@ fattn_status fwd_impl(const void* q, const void* k, const void* v, void* o, floa
   if (launch_prefill(p, tq, tk, tv, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_after(stream, FATTN_OK);
 }
 
 fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -289,7 +321,7 @@ fattn_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   if (launch_backward(p, tq, tk, tv, tdo, tdq, status, wait_timeout_ns(), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_after(stream, FATTN_OK);
 }
 
 }  // namespace
@@ -439,7 +471,7 @@ fattn_status fattn_decode_masked(const void* q, const void* k_cache, const void*
                                           align_up(parts * d * sizeof(float), 256));
   DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, key_lo};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_after(stream, FATTN_OK);
 }
 
 fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
@@ -463,7 +495,7 @@ fattn_status fattn_decode(const void* q, const void* k_cache, const void* v_cach
                                           align_up(parts * d * sizeof(float), 256));
   DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, 0};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_after(stream, FATTN_OK);
 }
 
 }  // extern "C"
@@ -502,7 +534,7 @@ fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   Fp8Problem p{q, k, workspace, o, lse, B, H, Nq, Nk, d, window_left, window_right, scale, q_descale, k_descale,
                v_descale, test_drop_kv_block()};
   if (launch_prefill_fp8(p, tq, tk, tvt, status, wait_timeout_ns(), s) != cudaSuccess) return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_after(stream, FATTN_OK);
 }
 
 }  // extern "C"
@@ -572,7 +604,7 @@ fattn_status fattn_decode_static(const void* q, const void* k_cache, const void*
   float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(parts * d * sizeof(float), 256));
   DecodeProblem p{q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, S, ws_o, ws_ml, 0};
   if (launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
-  return FATTN_OK;
+  return debug_after(stream, FATTN_OK);
 }
 
 fattn_status fattn_fwd_recomputed_rows(unsigned long long* out) {
@@ -595,7 +627,29 @@ fattn_status fattn_last_error(void* stream) {
     if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return FATTN_ERR_CUDA;
   }
+#ifdef FATTN_DEBUG
+  unsigned int rules = 0;
+  unsigned long long first = 0;
+  if (debug_collect(&rules, &first, false) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (rules != 0) return FATTN_ERR_DEBUG;
+#endif
   return (h & kStatusTimeout) ? FATTN_ERR_TIMEOUT : FATTN_OK;
+}
+
+int fattn_debug_build(void) {
+#ifdef FATTN_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+fattn_status fattn_debug_take(unsigned int* rules, unsigned long long* first) {
+  if (rules == nullptr || first == nullptr) return FATTN_ERR_INVALID_ARG;
+#ifdef FATTN_DEBUG
+  if (cudaDeviceSynchronize() != cudaSuccess) return FATTN_ERR_CUDA;
+#endif
+  return debug_collect(rules, first, true) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 }  // extern "C"

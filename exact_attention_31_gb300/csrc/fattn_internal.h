@@ -92,6 +92,19 @@ cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUt
 
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
 
+// Debug builds (-DFATTN_DEBUG): each kernel file's record of device-side checks that failed (the
+// rule bits, and the first failure as block << 32 | thread << 8 | rule + 1), read and optionally
+// cleared; release builds report zeros.
+cudaError_t debug_take_prefill(unsigned int* rules, unsigned long long* first, bool clear);
+cudaError_t debug_take_fp8(unsigned int* rules, unsigned long long* first, bool clear);
+cudaError_t debug_take_backward(unsigned int* rules, unsigned long long* first, bool clear);
+cudaError_t debug_take_decode(unsigned int* rules, unsigned long long* first, bool clear);
+// All files' records combined (rules OR-ed, the first non-empty first-failure record).
+cudaError_t debug_collect(unsigned int* rules, unsigned long long* first, bool clear);
+// Debug builds: wait for `stream` after a call's launches and turn a failed device-side check into
+// FATTN_ERR_DEBUG (the records stay for fattn_debug_take).  Release builds return `s` unchanged.
+fattn_status debug_after(void* stream, fattn_status s);
+
 // Element-mask summary.  The mask is judged per 128 x 128 tile (query rows 128 i.., keys 128 j..,
 // inside Nq x Nk) once per slice: one slice per (b, h) the mask's strides tell apart (a zero stride
 // shares a slice), slice (b' * nh + h') with b' = mask_sb ? b : 0, h' = mask_sh ? h : 0 and

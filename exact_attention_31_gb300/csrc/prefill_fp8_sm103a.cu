@@ -337,7 +337,8 @@ __device__ __forceinline__ bool softmax_unit(int t, int jb, int n_tiles, int row
     if (lane == 0) mbar_arrive(sbar + 8 * (C::kPFull + t));
   }
   if (!ok) return false;
-  const bool store = q_row < a.Nq;
+  const bool store =
+      q_row < a.Nq && dbg_in(static_cast<long long>(bh) * a.Nq + q_row, static_cast<long long>(a.BH) * a.Nq);
   __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
   if (n_tiles == 0) {
     if (store) {
@@ -458,6 +459,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate, uint32_t lead) {
+  FATTN_DBG_SKIP_IF(dbg_mma_d(d_tmem, idesc));
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
@@ -467,6 +469,7 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
 }
 __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate, uint32_t lead) {
+  FATTN_DBG_SKIP_IF(dbg_mma_d(d_tmem, idesc) | ((a_tmem & 0xFFFFu) + 8u > kTmemColumns ? kDbgTmemCol : 0u));
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
@@ -753,5 +756,8 @@ cudaError_t launch_prefill_fp8(const Fp8Problem& p, const CUtensorMap& tq, const
   if (p.d == 64) return launch_fp8_d<64>(a, tq, tk, tvt, stream);
   return cudaErrorInvalidValue;
 }
+
+// Debug builds: read (and optionally clear) this file's device-side check record.
+FATTN_DEBUG_ACCESSOR(fp8)
 
 }  // namespace fattn

@@ -629,7 +629,8 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
     }
   }
   if (!ok) return false;
-  const bool store = q_row < a.Nq;
+  const bool store =
+      q_row < a.Nq && dbg_in(static_cast<long long>(bh) * a.Nq + q_row, static_cast<long long>(a.BH) * a.Nq);
   __nv_bfloat16* orow = a.o + (static_cast<size_t>(bh) * a.Nq + (store ? q_row : 0)) * D;
   if (n_tiles == 0) {
     // No key is visible to any row of this tile: o = 0, L = log(0) = -inf.
@@ -1271,5 +1272,8 @@ cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUt
   if (p.d == 64) return launch_d<64, false>(p, tq, tk, tv, status, timeout_ns, stream);
   return launch_d<128, false>(p, tq, tk, tv, status, timeout_ns, stream);
 }
+
+// Debug builds: read (and optionally clear) this file's device-side check record.
+FATTN_DEBUG_ACCESSOR(prefill)
 
 }  // namespace fattn

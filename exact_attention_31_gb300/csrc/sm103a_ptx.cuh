@@ -5,9 +5,117 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace fattn {
+
+// ---------------------------------------------------------------------------------------------
+// Debug builds (compiled with -DFATTN_DEBUG).  The wrappers below check their operands against
+// rules the hardware enforces before they issue: shared-memory and barrier alignment, TMA
+// coordinates (the innermost coordinate of a tiled copy must address a multiple of 16 bytes, and a
+// store or reduce may not start at a negative coordinate), the 32-lane quarter of tensor memory a
+// warp may access and the 512 columns each kernel allocates.  A broken rule is recorded in the
+// translation unit's debug record (the rule's bit, and the first failure's block, thread and rule)
+// and the instruction is not issued, so a bad operand is reported instead of faulting the GPU; a
+// copy left out leaves its barrier incomplete, and the bounded waits then end the kernel.  Kernels
+// check their global stores against their outputs' extents the same way.  The host reads the
+// records with fattn_debug_take.  Release builds compile every check out.
+// ---------------------------------------------------------------------------------------------
+enum DebugRule : uint32_t {
+  kDbgSmemAlign = 1u << 0,  // shared-memory operand or barrier address not aligned
+  kDbgTmaCoord = 1u << 1,   // TMA innermost coordinate not a multiple of 16 elements, or a store/reduce below 0
+  kDbgTmemLane = 1u << 2,   // tcgen05.ld/st/mma address outside the lanes the warp (or the MMA) may use
+  kDbgTmemCol = 1u << 3,    // tensor-memory columns past the 512 allocated
+  kDbgBulk = 1u << 4,       // untiled bulk copy: size or global address not a multiple of 16 bytes
+  kDbgGlobal = 1u << 5,     // a kernel's global store outside its output
+};
+constexpr uint32_t kTmemColumns = 512;
+
+// The rules as pure functions of the operands (host and device): each returns the rules the
+// operands break, 0 when they break none.  Every TMA coordinate this library issues along the
+// innermost dimension is a multiple of 16 elements, which is 16-byte aligned for every element
+// size it uses (1, 2 and 4 bytes); tiled copies land on 128-byte aligned shared memory.
+__host__ __device__ constexpr uint32_t dbg_bar(uint32_t bar) { return (bar & 7u) ? kDbgSmemAlign : 0u; }
+__host__ __device__ constexpr uint32_t dbg_tma_tile(uint32_t smem, uint32_t bar, int x, int y, int z, bool store) {
+  return ((smem & 127u) ? kDbgSmemAlign : 0u) | (store ? 0u : dbg_bar(bar)) | ((x & 15) ? kDbgTmaCoord : 0u) |
+         ((store && (x < 0 || y < 0 || z < 0)) ? kDbgTmaCoord : 0u);
+}
+__host__ __device__ constexpr uint32_t dbg_bulk(uint32_t smem, uint64_t gaddr, uint32_t bytes, uint32_t bar) {
+  return ((smem & 15u) ? kDbgSmemAlign : 0u) | dbg_bar(bar) | (((gaddr & 15u) || (bytes & 15u) || bytes == 0u) ? kDbgBulk : 0u);
+}
+// tcgen05.ld/st by warp `warp` of its CTA: lanes 32 (warp % 4) .. + 31, columns [col, col + cols).
+__host__ __device__ constexpr uint32_t dbg_tmem(uint32_t taddr, uint32_t cols, uint32_t warp) {
+  return ((taddr >> 16) != 32u * (warp & 3u) ? kDbgTmemLane : 0u) |
+         ((taddr & 0xFFFFu) + cols > kTmemColumns ? kDbgTmemCol : 0u);
+}
+// tcgen05.mma with M = 128: the accumulator starts at lane 0 and spans the instruction's N columns
+// (N / 8 in bits 17-22 of the instruction descriptor).
+__host__ __device__ constexpr uint32_t dbg_mma_d(uint32_t d_tmem, uint32_t idesc) {
+  return ((d_tmem >> 16) != 0u ? kDbgTmemLane : 0u) |
+         ((d_tmem & 0xFFFFu) + ((idesc >> 17) & 0x3Fu) * 8u > kTmemColumns ? kDbgTmemCol : 0u);
+}
+static_assert(dbg_tma_tile(1024, 8, 64, -3, 0, false) == 0 && dbg_tma_tile(1040, 8, 0, 0, 0, false) == kDbgSmemAlign &&
+                  dbg_tma_tile(1024, 12, 0, 0, 0, false) == kDbgSmemAlign &&
+                  dbg_tma_tile(1024, 8, 8, 0, 0, false) == kDbgTmaCoord &&
+                  dbg_tma_tile(1024, 0, 32, -1, 0, true) == kDbgTmaCoord && dbg_tma_tile(1024, 0, 32, 5, 2, true) == 0,
+              "TMA rules");
+static_assert(dbg_bulk(16, 32, 4096, 8) == 0 && dbg_bulk(8, 32, 4096, 8) == kDbgSmemAlign &&
+                  dbg_bulk(16, 40, 4096, 8) == kDbgBulk && dbg_bulk(16, 32, 4100, 8) == kDbgBulk,
+              "bulk rules");
+static_assert(dbg_tmem((64u << 16) | 480u, 32, 6) == 0 && dbg_tmem((64u << 16) | 481u, 32, 6) == kDbgTmemCol &&
+                  dbg_tmem((32u << 16), 32, 6) == kDbgTmemLane && dbg_tmem((96u << 16) | 16u, 16, 11) == 0,
+              "tensor-memory rules");
+static_assert(dbg_mma_d(384u, (128u >> 3) << 17) == 0 && dbg_mma_d(448u, (128u >> 3) << 17) == kDbgTmemCol &&
+                  dbg_mma_d((32u << 16) | 0u, (64u >> 3) << 17) == kDbgTmemLane,
+              "MMA accumulator rules");
+
+#ifdef FATTN_DEBUG
+// This translation unit's debug record.
+static __device__ unsigned int g_fattn_dbg_rules;        // OR of the rules broken
+static __device__ unsigned long long g_fattn_dbg_first;  // first failure: block << 32 | thread << 8 | rule + 1
+static __device__ __noinline__ void dbg_record(uint32_t rules) {
+  atomicOr(&g_fattn_dbg_rules, rules);
+  const unsigned long long rec = (static_cast<unsigned long long>(blockIdx.x) << 32) |
+                                 (static_cast<unsigned long long>(threadIdx.x) << 8) |
+                                 static_cast<unsigned long long>(__ffs(static_cast<int>(rules)));
+  atomicCAS(&g_fattn_dbg_first, 0ull, rec);
+}
+static __device__ __forceinline__ bool dbg_fails(uint32_t rules) {
+  if (rules == 0u) return false;
+  dbg_record(rules);
+  return true;
+}
+// Skip the rest of the calling wrapper when its operands break a rule.
+#define FATTN_DBG_SKIP_IF(rules) \
+  if (::fattn::dbg_fails(rules)) return
+// A global store of element `index` into an output of `count` elements: false (recorded) outside.
+static __device__ __forceinline__ bool dbg_in(long long index, long long count) {
+  return !dbg_fails(index >= 0 && index < count ? 0u : kDbgGlobal);
+}
+// Host accessor of the record, defined once in each translation unit that has kernels.
+#define FATTN_DEBUG_ACCESSOR(name)                                                                      \
+  cudaError_t debug_take_##name(unsigned int* rules, unsigned long long* first, bool clear) {           \
+    cudaError_t e = cudaMemcpyFromSymbol(rules, g_fattn_dbg_rules, sizeof(unsigned int));             \
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(first, g_fattn_dbg_first, sizeof(unsigned long long)); \
+    if (e == cudaSuccess && clear) {                                                                  \
+      const unsigned int r0 = 0u;                                                                     \
+      const unsigned long long f0 = 0ull;                                                             \
+      e = cudaMemcpyToSymbol(g_fattn_dbg_rules, &r0, sizeof r0);                                      \
+      if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fattn_dbg_first, &f0, sizeof f0);                \
+    }                                                                                                 \
+    return e;                                                                                         \
+  }
+#else
+#define FATTN_DBG_SKIP_IF(rules)
+static __device__ __forceinline__ constexpr bool dbg_in(long long, long long) { return true; }
+#define FATTN_DEBUG_ACCESSOR(name)                                                            \
+  cudaError_t debug_take_##name(unsigned int* rules, unsigned long long* first, bool) {       \
+    *rules = 0u;                                                                            \
+    *first = 0ull;                                                                          \
+    return cudaSuccess;                                                                     \
+  }
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -23,6 +131,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // mbarrier
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  FATTN_DBG_SKIP_IF(dbg_bar(bar));
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
@@ -31,16 +140,21 @@ __device__ __forceinline__ void fence_mbarrier_init() {
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  FATTN_DBG_SKIP_IF(dbg_bar(bar));
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  FATTN_DBG_SKIP_IF(dbg_bar(bar));
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
                : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+#ifdef FATTN_DEBUG
+  if (dbg_fails(dbg_bar(bar))) return true;  // reported, not waited on
+#endif
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -78,6 +192,7 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
                                             int y, int z) {
+  FATTN_DBG_SKIP_IF(dbg_tma_tile(dst, bar, x, y, z, false));
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
@@ -87,6 +202,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 // Untiled bulk copy global -> shared completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  FATTN_DBG_SKIP_IF(dbg_bulk(dst, reinterpret_cast<uint64_t>(src), bytes, bar));
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
@@ -96,6 +212,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Element-wise fp32 add of a shared-memory box into global memory through a 3-D tensor map
 // (TMA reduce); tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  FATTN_DBG_SKIP_IF(dbg_tma_tile(src, 0u, x, y, z, true));
   asm volatile(
       "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
@@ -165,6 +282,12 @@ __device__ __forceinline__ void tmem_wait_st() {
 // Warp-wide: each lane reads 32 consecutive 32-bit columns of its own TMEM lane.  The lane field
 // of `taddr` must be the warp's 32-lane quarter.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+#ifdef FATTN_DEBUG
+  if (dbg_fails(dbg_tmem(taddr, 32, threadIdx.x >> 5))) {
+    for (int i = 0; i < 32; ++i) r[i] = 0u;
+    return;
+  }
+#endif
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -178,6 +301,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  FATTN_DBG_SKIP_IF(dbg_tmem(taddr, 32, threadIdx.x >> 5));
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
@@ -190,6 +314,7 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  FATTN_DBG_SKIP_IF(dbg_tmem(taddr, 16, threadIdx.x >> 5));
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
@@ -253,6 +378,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr) {
 // D[tmem] (+)= A[smem] * B[smem]^T
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
+  FATTN_DBG_SKIP_IF(dbg_mma_d(d_tmem, idesc));
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -264,6 +390,7 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
+  FATTN_DBG_SKIP_IF(dbg_mma_d(d_tmem, idesc) | ((a_tmem & 0xFFFFu) + 8u > kTmemColumns ? kDbgTmemCol : 0u));
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -278,6 +405,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // tensor core's own rate.
 __device__ __forceinline__ void mma_ss_lead(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate, uint32_t lead) {
+  FATTN_DBG_SKIP_IF(dbg_mma_d(d_tmem, idesc));
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
@@ -288,6 +416,7 @@ __device__ __forceinline__ void mma_ss_lead(uint32_t d_tmem, uint64_t a_desc, ui
 
 __device__ __forceinline__ void mma_ts_lead(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate, uint32_t lead) {
+  FATTN_DBG_SKIP_IF(dbg_mma_d(d_tmem, idesc) | ((a_tmem & 0xFFFFu) + 8u > kTmemColumns ? kDbgTmemCol : 0u));
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
@@ -297,6 +426,7 @@ __device__ __forceinline__ void mma_ts_lead(uint32_t d_tmem, uint32_t a_tmem, ui
 }
 
 __device__ __forceinline__ void mma_commit_lead(uint32_t bar, uint32_t lead) {
+  FATTN_DBG_SKIP_IF(dbg_bar(bar));
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
       "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
@@ -315,6 +445,7 @@ __device__ __forceinline__ uint32_t elect_lane() {
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
+  FATTN_DBG_SKIP_IF(dbg_bar(bar));
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");

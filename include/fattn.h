@@ -39,7 +39,8 @@ typedef enum fattn_status {
   FATTN_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, a non-positive size, a bad scale ... */
   FATTN_ERR_UNSUPPORTED = 2, /* a head dimension other than 64 or 128 */
   FATTN_ERR_CUDA = 3,        /* the CUDA runtime refused a launch or an attribute call */
-  FATTN_ERR_TIMEOUT = 4      /* a bounded on-device wait gave up (see fattn_last_error) */
+  FATTN_ERR_TIMEOUT = 4,     /* a bounded on-device wait gave up (see fattn_last_error) */
+  FATTN_ERR_DEBUG = 5        /* debug builds only: a device-side check failed (see fattn_debug_take) */
 } fattn_status;
 
 /*
@@ -357,6 +358,30 @@ fattn_status fattn_last_error(void* stream);
  * (FATTN_ERR_INVALID_ARG); FATTN_ERR_CUDA if the device reported an error.
  */
 fattn_status fattn_fwd_recomputed_rows(unsigned long long* out);
+
+/*
+ * Debug builds.  The library can be built with device-side checks (libfattn_debug.so, compiled with
+ * -DFATTN_DEBUG): before every TMA copy, bulk copy, mbarrier operation, tensor-memory load or store
+ * and tcgen05.mma the kernels check the operands against the hardware's rules (shared-memory and
+ * barrier alignment; a TMA copy's innermost coordinate a multiple of 16 elements, and no store or
+ * reduce starting below 0; a warp's tensor-memory accesses inside its 32-lane quarter and the 512
+ * allocated columns), and every output store against its tensor's extent.  An operation that
+ * breaks a rule is not issued; the rule is recorded instead, so that a bad index is reported and
+ * does not fault the GPU (a copy left out leaves its barrier incomplete, and the bounded waits end
+ * the kernel).  In debug builds every entry point waits for its stream after launching and returns
+ * FATTN_ERR_DEBUG when a check failed, and fattn_last_error reports it too.  The arithmetic is the
+ * release build's: results are bit-identical.
+ *
+ * fattn_debug_build -- 1 for a library built with the device-side checks, 0 otherwise.
+ * fattn_debug_take  -- (debug builds: wait for the device, then) read and clear the checks' record:
+ *   *rules = the OR of the rules broken since the last call (bit 0 shared-memory or barrier
+ *   alignment, bit 1 TMA coordinate, bit 2 tensor-memory lane, bit 3 tensor-memory column, bit 4
+ *   bulk-copy size or address, bit 5 output store out of range), *first = the first failure as
+ *   block << 32 | thread << 8 | (index of its lowest rule bit + 1), 0 if none.  Release builds
+ *   report 0 and 0 and touch no device.  FATTN_ERR_INVALID_ARG for a NULL pointer.
+ */
+int fattn_debug_build(void);
+fattn_status fattn_debug_take(unsigned int* rules, unsigned long long* first);
 
 /* fattn_status_string -- a static, human-readable name for a status code (never NULL). */
 const char* fattn_status_string(int status);
