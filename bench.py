@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -322,6 +323,23 @@ def host_inputs_f64(seed_prefill=0xFA77E004, seed_decode_pairs=0xFA77E005):
     return pf, df
 
 
+def host_cpu():
+    """The host the oracle ran on: its logical CPU count and model name (from /proc/cpuinfo, which
+    names the part on x86 and gives the implementer and part numbers on Arm)."""
+    info = {"cpu_count": os.cpu_count(), "machine": platform.machine()}
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+        for key in ("model name", "Model name", "CPU implementer", "CPU part"):
+            for line in text.splitlines():
+                if line.split(":")[0].strip() == key:
+                    info[key.lower().replace(" ", "_")] = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return info
+
+
 def cpu_baseline(budget_s=12.0):
     pf, df = host_inputs_f64()
     flops, secs, rows, threads = oracle_prefill_sample(*pf, budget_s=budget_s * 0.6)
@@ -337,6 +355,7 @@ def cpu_baseline(budget_s=12.0):
         "decode_gbs": kvb / dsecs / 1e9,
         "value_1core": flops1 / secs1 / 1e12,
         "sample_1core": f"{rows1} random query rows of the same prefill on one host thread ({secs1:.1f} s)",
+        "host": host_cpu(),
     }
 
 
@@ -479,6 +498,8 @@ def run_ours(args):
             "l2": ("prefill inputs (96 MiB) are below L2, so a 512 MiB buffer is written before every "
                    "prefill (inside ms_per_step, outside the per-kernel events); the decode reads 8 GiB"),
             "parallelism": f"replicas x{world}",
+            "seeds": {"prefill": hex(0xFA77E000 + 4), "decode": hex(0xFA77E000 + 5),
+                      "generator": "torch.Generator per tensor; N(0,1) in fp32 rounded to bf16"},
         },
     })
     if do_prefill:
