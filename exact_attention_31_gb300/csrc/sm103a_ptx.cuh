@@ -42,7 +42,8 @@ __host__ __device__ constexpr uint32_t dbg_tma_tile(uint32_t smem, uint32_t bar,
          ((store && (x < 0 || y < 0 || z < 0)) ? kDbgTmaCoord : 0u);
 }
 __host__ __device__ constexpr uint32_t dbg_bulk(uint32_t smem, uint64_t gaddr, uint32_t bytes, uint32_t bar) {
-  return ((smem & 15u) ? kDbgSmemAlign : 0u) | dbg_bar(bar) | (((gaddr & 15u) || (bytes & 15u) || bytes == 0u) ? kDbgBulk : 0u);
+  return ((smem & 15u) ? kDbgSmemAlign : 0u) | dbg_bar(bar) |
+         (((gaddr & 15u) || (bytes & 15u) || bytes == 0u) ? kDbgBulk : 0u);
 }
 // tcgen05.ld/st by warp `warp` of its CTA: lanes 32 (warp % 4) .. + 31, columns [col, col + cols).
 __host__ __device__ constexpr uint32_t dbg_tmem(uint32_t taddr, uint32_t cols, uint32_t warp) {

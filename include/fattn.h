@@ -354,7 +354,8 @@ fattn_status fattn_last_error(void* stream);
 /*
  * fattn_fwd_recomputed_rows -- the number of rows of fattn_fwd and fattn_fwd_masked that failed the
  * fast path's range check on the current device since the library was loaded, and whose query
- * tiles were therefore computed again with a running max (a diagnostic; see fattn_fwd, Numerics).  Waits for all work on the current device first.  *out must not be NULL
+ * tiles were therefore computed again with a running max (a diagnostic; see fattn_fwd, Numerics).
+ * Waits for all work on the current device first.  *out must not be NULL
  * (FATTN_ERR_INVALID_ARG); FATTN_ERR_CUDA if the device reported an error.
  */
 fattn_status fattn_fwd_recomputed_rows(unsigned long long* out);
