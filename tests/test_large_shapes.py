@@ -1,6 +1,7 @@
 """GPU parity at size extremes the other tests do not reach: long sequences (a 32K-token causal
-prefill, a 256K-key decode), many heads in one call, and the FP8 forward at 16K tokens.  Outputs are
-compared with the fp64 oracle on sampled rows, at the tolerances of the regular parity tests; these
+prefill, a 256K-key decode, the backward at 8K tokens, an element mask over 32K keys), many heads
+in one call, and the FP8 forward at 16K tokens.  Outputs are compared with the fp64 oracle on
+sampled rows (every gradient of one 8K head), at the tolerances of the regular parity tests; these
 catch 32-bit index overflows and scheduling edge cases of the persistent grid and the split count.
 """
 
@@ -81,3 +82,55 @@ def test_fp8_16k_tokens_causal(fa):
     rows = np.concatenate([bh * N + per_head for bh in range(B * H)])
     check_bound(o, lse, _deq(q8, qs), _deq(k8, ks), _deq(v8, vs), (-1, 0), 1 / math.sqrt(d), rows=rows,
                 what="fp8 N=16384")
+
+
+def test_backward_8k_tokens_causal(fa):
+    # one head of 8192 tokens: 64 key-tile CTAs, the longest walking 64 query tiles; every gradient
+    # against the oracle's (one head is one oracle thread: about half a minute), relative to its
+    # magnitude as in the regular backward tests
+    from exact_attention_31_gb300.workloads import make_dout, make_qkv
+    from test_backward_parity import GRAD_MAX_REL, GRAD_MEAN_REL
+    B, H, N, d = 1, 1, 8192, 64
+    q, k, v, _ = make_qkv(B, H, N, N, d, 9504, device="cuda")
+    do = make_dout(B, H, N, d, 9504, device="cuda")
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.fattn_fwd(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.fattn_bwd(q, k, v, o, lse, do, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    refs = oracle.attention_backward(to64(q), to64(k), to64(v), to64(do), causal=True, scale=scale)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        err = np.abs(to64(got) - ref)
+        assert err.max() <= GRAD_MAX_REL * np.abs(ref).max(), (name, err.max(), np.abs(ref).max())
+        assert err.mean() <= GRAD_MEAN_REL * np.abs(ref).mean(), (name, err.mean(), np.abs(ref).mean())
+
+
+def test_element_mask_32k_keys(fa):
+    # 4096 queries against 32,768 keys under one mask for both heads: block-sparse (a seeded half of
+    # the 128 x 128 blocks hidden) with random bits inside one block in eight, and a row that sees
+    # nothing; the summary's bit words span four 64-bit words per query tile
+    from exact_attention_31_gb300.workloads import make_qkv
+    B, H, Nq, Nk, d = 1, 2, 4096, 32768, 64
+    q, k, v, _ = make_qkv(B, H, Nq, Nk, d, 9505, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(9505)
+    blocks = torch.rand((Nq // 128, Nk // 128), generator=g, device="cuda") < 0.5
+    part = torch.rand((Nq // 128, Nk // 128), generator=g, device="cuda") < 0.125
+    mask = blocks.repeat_interleave(128, 0).repeat_interleave(128, 1)
+    noise = torch.rand((Nq, Nk), generator=g, device="cuda") < 0.5
+    mask = torch.where(part.repeat_interleave(128, 0).repeat_interleave(128, 1), mask & noise, mask)
+    mask[1000] = False
+    del noise
+    o, lse = fa.fattn_fwd(q, k, v, scale=0.125, mask=fa.pack_mask(mask))
+    torch.cuda.synchronize()
+    assert fa.fattn_last_error() == 0
+    per_head = np.array([0, 1, 127, 128, 999, 1000, 1001, 2047, 2048, 4095])
+    rows = np.concatenate([bh * Nq + per_head for bh in range(B * H)])
+    m = mask.cpu().numpy()
+    o_ref, lse_ref = oracle.attention_rows(to64(q), to64(k), to64(v), rows, scale=0.125, mask=m)
+    o_k = to64(o).reshape(-1, d)[rows]
+    l_k = to64(lse).reshape(-1)[rows]
+    empty = np.isin(rows % Nq, [1000])
+    assert np.all(o_k[empty] == 0.0) and np.all(l_k[empty] == -np.inf)
+    err = np.abs(o_k[~empty] - o_ref[~empty])
+    assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (err.max(), err.mean())
+    assert np.abs(l_k[~empty] - lse_ref[~empty]).max() <= LSE_MAX_ABS
