@@ -476,8 +476,7 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
     }
     tc_fence_after();
     uint32_t s[4][32];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x32(tS + 32 * h, s[h]);
+    tmem_ld_32x32b_x128(tS, s);  // one load of the 128 columns (fewer than four 32-column loads)
 #pragma unroll
     for (int h = 0; h < 4; ++h) wait_dep(s[h]);
     if constexpr (C::kSepP) {
@@ -649,11 +648,14 @@ __device__ __forceinline__ bool softmax_unit(int t, int k, int jb, int n_tiles, 
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
   // Sum of the outputs / 256 (not finite iff one of them is not), in four independent partial sums.
   float fin = 0.f, fin1 = 0.f, fin2 = 0.f, fin3 = 0.f;
+  uint32_t oall[D / 32][32];  // O_t's D columns of this row, in one load
+  if constexpr (D == 128) tmem_ld_32x32b_x128(tO, oall);
+  else tmem_ld_32x32b_x64(tO, oall);
+#pragma unroll
+  for (int h = 0; h < D / 32; ++h) wait_dep(oall[h]);
 #pragma unroll
   for (int h = 0; h < D / 32; ++h) {
-    uint32_t o[32];
-    tmem_ld_32x32b_x32(tO + 32 * h, o);
-    wait_dep(o);
+    const uint32_t(&o)[32] = oall[h];
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
