@@ -135,6 +135,10 @@ struct Args {
   const unsigned long long* tiles;
   long long tiles_sb, tiles_sh;
   int tiles_w;
+  // One-tile items: the units from half_unit0 on are taken one query tile at a time, item
+  // half_unit0 + s being tile s % 2 of unit half_unit0 + s / 2 (unit_end counts items); the other
+  // tile is another CTA's and is marked absent (je < jb).  half_unit0 = unit_end: none.
+  int half_unit0;
 };
 
 // Key/value tiles [jb, je) that query tile [r0, r0 + 128) must visit: those holding a key visible to
@@ -245,16 +249,32 @@ __device__ __forceinline__ int live_count(const Args& a, const Unit& u, int t) {
 // The k-th unit of this CTA.  The grid is persistent (at most one CTA per SM); units are taken in
 // rounds of gridDim.x, heaviest causal units (last query rows) first, and every other round is
 // walked backwards so that each CTA's total is closer to the others'.  Returns false past the end.
-template <bool M>
+template <bool M, bool H>
 __device__ __forceinline__ bool cta_unit(int k, const Args& a, Unit& u) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = a.unit_base + static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
   if (idx >= a.unit_end) return false;
-  const int i = static_cast<int>(idx);
+  int i = static_cast<int>(idx);
+  int keep = -1;  // a one-tile item: the query tile it computes
+  if constexpr (H) {
+    if (i >= a.half_unit0) {
+      keep = (i - a.half_unit0) & 1;
+      i = a.half_unit0 + ((i - a.half_unit0) >> 1);
+    }
+  }
   u.bh = i % a.BH;
   u.row0 = (a.units_per_head - 1 - i / a.BH) * kTiles * kBlockM;
   key_tiles(u.row0, a, u.jb[0], u.je[0]);
   key_tiles(u.row0 + kBlockM, a, u.jb[1], u.je[1]);
+  if constexpr (H) {
+    if (keep == 0) {
+      u.jb[1] = 0;
+      u.je[1] = -1;
+    } else if (keep == 1) {
+      u.jb[0] = 0;
+      u.je[0] = -1;
+    }
+  }
   if constexpr (M) {
     // Narrow each range to its first and last key tile with a visible key; a tile left with none
     // is empty (its rows get o = 0 and L = -inf).
@@ -706,12 +726,12 @@ __device__ __noinline__ bool softmax_unit_running(int t, int k, int jb, int n_ti
   return softmax_unit<D, M, true>(t, k, jb, n_tiles, row0, bh, tmem, sbar, a, ab, g, done);
 }
 
-template <int D, bool M>
+template <int D, bool M, bool H>
 __device__ __noinline__ void softmax_tail(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab, int g,
                                           int done, uint32_t* redo, bool ok) {
   if (!redo_begin(ok, ab.flag)) return;
   Unit u;
-  for (int k = 0; cta_unit<M>(k, a, u); ++k) {
+  for (int k = 0; cta_unit<M, H>(k, a, u); ++k) {
     if (!redo_unit(k, redo, u) || u.je[t] == u.jb[t]) continue;
     ab.renew(a.timeout_ns);
     if (!softmax_unit_running<D, M>(t, k, u.jb[t], live_count<M>(a, u, t), u.row0, u.bh, tmem, sbar, a, ab, g, done))
@@ -719,20 +739,23 @@ __device__ __noinline__ void softmax_tail(int t, uint32_t tmem, uint32_t sbar, c
   }
 }
 
-template <int D, bool M>
+template <int D, bool M, bool H>
 __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbar, const Args& a, Abort ab,
                                              uint32_t* redo) {
   int g = 0, done = 0;
   bool ok = true;
   Unit u;
-  for (int k = 0; cta_unit<M>(k, a, u); ++k) {
+  for (int k = 0; cta_unit<M, H>(k, a, u); ++k) {
+    if constexpr (H) {
+      if (u.je[t] < u.jb[t]) continue;  // a one-tile item's other tile: another CTA's rows
+    }
     ab.renew(a.timeout_ns);
     if (!softmax_unit<D, M, false>(t, k, u.jb[t], live_count<M>(a, u, t), u.row0, u.bh, tmem, sbar, a, ab, g, done)) {
       ok = false;
       break;
     }
   }
-  softmax_tail<D, M>(t, tmem, sbar, a, ab, g, done, redo, ok);
+  softmax_tail<D, M, H>(t, tmem, sbar, a, ab, g, done, redo, ok);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -755,7 +778,7 @@ __device__ __forceinline__ bool producer_unit(const Unit& u, const CUtensorMap* 
   const uint32_t sbar = sbase + C::kBarOff;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
-    if (u.je[t] == u.jb[t]) continue;
+    if (u.je[t] <= u.jb[t]) continue;  // empty, or (a one-tile item) another CTA's
     // Q_t's buffer is free once the previous unit's last S_t has read it.
     if (ps.qloads[t] > 0 && !thread_wait(sbar + 8 * (C::kQFree + t), (ps.qloads[t] - 1) & 1, ab)) return false;
     const uint32_t bar = sbar + 8 * (C::kQFull + t);
@@ -802,7 +825,7 @@ __device__ __noinline__ bool producer_unit_redo(const Unit& u, const CUtensorMap
 
 // The producer's redo phase and wind-down (whole warp; lane 0 issues).  After a wait gave up, the
 // copies already in flight land before the CTA's shared memory goes away.
-template <int D, bool M>
+template <int D, bool M, bool H>
 __device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                            uint32_t sbase, const Args& a, Abort ab, ProducerState ps, bool ok,
                                            uint32_t* redo) {
@@ -811,7 +834,7 @@ __device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensor
   const bool lead = (threadIdx.x & 31) == 0;
   if (redo_begin(ok, ab.flag) && lead) {
     Unit u;
-    for (int k = 0; cta_unit<M>(k, a, u); ++k) {
+    for (int k = 0; cta_unit<M, H>(k, a, u); ++k) {
       if (!redo_unit(k, redo, u)) continue;
       ab.renew(a.timeout_ns);
       if (!producer_unit_redo<D, M>(u, tq, tk, tv, sbase, a, ab, ps)) {
@@ -836,7 +859,7 @@ __device__ __noinline__ void producer_tail(const CUtensorMap* tq, const CUtensor
 }
 
 // Whole warp; lane 0 issues the main phase's loads.
-template <int D, bool M>
+template <int D, bool M, bool H>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                               uint32_t sbase, const Args& a, Abort ab, uint32_t* redo) {
   ProducerState ps;
@@ -846,7 +869,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
     tma_prefetch_desc(tk);
     tma_prefetch_desc(tv);
     Unit u;
-    for (int k = 0; cta_unit<M>(k, a, u); ++k) {
+    for (int k = 0; cta_unit<M, H>(k, a, u); ++k) {
       ab.renew(a.timeout_ns);
       if (!producer_unit<D, M>(u, tq, tk, tv, sbase, a, ab, ps)) {
         ok = false;
@@ -855,7 +878,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
     }
   }
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  producer_tail<D, M>(tq, tk, tv, sbase, a, ab, ps, ok, redo);
+  producer_tail<D, M, H>(tq, tk, tv, sbase, a, ab, ps, ok, redo);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1089,13 +1112,13 @@ __device__ __noinline__ bool mma_unit_redo(int tt, const Unit& u, const MmaCtx<D
 // The MMA warp's redo phase and wind-down: before the CTA winds down, every MMA (and every arrival
 // its commits make on this CTA's barriers) has completed, on the normal path and after a timeout
 // alike.
-template <int D, bool M>
+template <int D, bool M, bool H>
 __device__ __noinline__ void mma_tail(int tt, const MmaCtx<D>& m, MmaState st, const Args& a, Abort ab, bool ok,
                                       uint32_t* redo) {
   using C = Cfg<D>;
   if (redo_begin(ok, ab.flag)) {
     Unit u;
-    for (int k = 0; ok && cta_unit<M>(k, a, u); ++k) {
+    for (int k = 0; ok && cta_unit<M, H>(k, a, u); ++k) {
       if (!redo_unit(k, redo, u)) continue;
       ab.renew(a.timeout_ns);
       ok = mma_unit_redo<D, M>(tt, u, m, st, ab, a);
@@ -1111,7 +1134,7 @@ __device__ __noinline__ void mma_tail(int tt, const MmaCtx<D>& m, MmaState st, c
 
 // Whole warp.  `tt` is the query tile of this warp (d = 64); with d = 128 the one MMA warp (tt = 0)
 // issues both tiles' products.
-template <int D, bool M>
+template <int D, bool M, bool H>
 __device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, const Args& a, Abort ab,
                                          uint32_t* redo) {
   using C = Cfg<D>;
@@ -1120,17 +1143,17 @@ __device__ __forceinline__ void mma_role(int tt, uint32_t tmem, uint32_t sbase, 
   MmaState st;
   bool ok = true;
   Unit u;
-  for (int k = 0; ok && cta_unit<M>(k, a, u); ++k) {
+  for (int k = 0; ok && cta_unit<M, H>(k, a, u); ++k) {
     ab.renew(a.timeout_ns);
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
       if ((!C::kSepP || t == tt) && u.je[t] > u.jb[t] && ok) ok = m.wait(C::kQFull + t, st.q_seen[t]++, ab);
     if (ok) ok = C::kSepP ? mma_unit_tile<D, M>(tt, u, m, st, ab, a) : mma_unit_aliased_p<D, M>(u, m, st, ab, a);
   }
-  mma_tail<D, M>(tt, m, st, a, ab, ok, redo);
+  mma_tail<D, M, H>(tt, m, st, a, ab, ok, redo);
 }
 
-template <int D, bool M>
+template <int D, bool M, bool H>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Args a) {
@@ -1180,13 +1203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each role works through the CTA's units, then meets the others at one barrier (redo_begin) and
   // computes the marked tiles again.
   if (warp < 8) {
-    softmax_role<D, M>(warp >> 2, tmem, sbar, a, ab, redo);
+    softmax_role<D, M, H>(warp >> 2, tmem, sbar, a, ab, redo);
   } else if (warp == kProducerWarp) {
-    producer_role<D, M>(&tm_q, &tm_k, &tm_v, sbase, a, ab, redo);
+    producer_role<D, M, H>(&tm_q, &tm_k, &tm_v, sbase, a, ab, redo);
   } else if (warp == kMmaWarp) {
-    mma_role<D, M>(0, tmem, sbase, a, ab, redo);
+    mma_role<D, M, H>(0, tmem, sbase, a, ab, redo);
   } else if (C::kSepP && warp == kMmaWarp1) {
-    mma_role<D, M>(1, tmem, sbase, a, ab, redo);
+    mma_role<D, M, H>(1, tmem, sbase, a, ab, redo);
   } else {
     redo_begin(true, abort_flag);  // (d = 128: the spare warp only takes part in the barrier)
   }
@@ -1199,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool M>
+template <int D, bool M, bool H>
 cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
                      cudaStream_t stream) {
@@ -1209,7 +1232,7 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel<D, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_kernel<D, M, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -1249,13 +1272,39 @@ cudaError_t launch_d(const FwdProblem& p, const CUtensorMap& tq, const CUtensorM
   // A CTA marks the tiles to compute again in a bitmask of kMaxUnitsPerCta units, so one launch
   // covers at most grid * kMaxUnitsPerCta units; larger problems take several launches.
   const long long total = static_cast<long long>(a.units_per_head) * a.BH;
-  const long long grid = std::min<long long>(total, sm_count[dev]);
+  const int sms = sm_count[dev];
+  // One-tile items where two-tile units would leave SMs idle: when there are fewer units than SMs,
+  // every unit is taken one query tile at a time; without a band (units of equal length), when the
+  // last round of units fills at most half of the SMs, that round's units are (under a band the
+  // last round holds the lightest units, and the rounds' balance is better left as it is).  A CTA
+  // with one tile computes it faster than its share of a unit, and each tile still writes its own O
+  // and L, so nothing is merged afterwards.  The kernel for them is a separate instantiation, so
+  // that the one for whole units is unchanged.  (Without an element mask only.)
+  long long half0 = total;
+  if (total <= kMaxUnitsPerCta * static_cast<long long>(sms)) {
+    if (2 * total <= sms) half0 = 0;
+    else if (total > sms && 2 * (total % sms) <= sms && p.window_left < 0 && p.window_right < 0)
+      half0 = total - total % sms;
+  }
+  if constexpr (!M && !H) {
+    if (half0 < total) return launch_d<D, false, true>(p, tq, tk, tv, status, timeout_ns, stream);
+  }
+  a.half_unit0 = static_cast<int>(std::min<long long>(half0, 0x7fffffffLL));
+  if constexpr (H) {
+    const long long items = total + (total - half0);
+    a.unit_base = 0;
+    a.unit_end = static_cast<int>(items);
+    prefill_kernel<D, M, H><<<static_cast<unsigned int>(std::min<long long>(items, sms)), kThreads,
+                              C::kSmemBytes, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+  }
+  const long long grid = std::min<long long>(total, sms);
   const long long per_launch = grid * kMaxUnitsPerCta;
   for (long long base = 0; base < total; base += per_launch) {
     a.unit_base = static_cast<int>(base);
     a.unit_end = static_cast<int>(std::min(total, base + per_launch));
     const unsigned int g = static_cast<unsigned int>(std::min<long long>(grid, a.unit_end - a.unit_base));
-    prefill_kernel<D, M><<<g, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+    prefill_kernel<D, M, H><<<g, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1268,11 +1317,11 @@ cudaError_t launch_prefill(const FwdProblem& p, const CUtensorMap& tq, const CUt
                            const CUtensorMap& tv, unsigned int* status, unsigned long long timeout_ns,
                            cudaStream_t stream) {
   if (p.tiles != nullptr) {
-    if (p.d == 64) return launch_d<64, true>(p, tq, tk, tv, status, timeout_ns, stream);
-    return launch_d<128, true>(p, tq, tk, tv, status, timeout_ns, stream);
+    if (p.d == 64) return launch_d<64, true, false>(p, tq, tk, tv, status, timeout_ns, stream);
+    return launch_d<128, true, false>(p, tq, tk, tv, status, timeout_ns, stream);
   }
-  if (p.d == 64) return launch_d<64, false>(p, tq, tk, tv, status, timeout_ns, stream);
-  return launch_d<128, false>(p, tq, tk, tv, status, timeout_ns, stream);
+  if (p.d == 64) return launch_d<64, false, false>(p, tq, tk, tv, status, timeout_ns, stream);
+  return launch_d<128, false, false>(p, tq, tk, tv, status, timeout_ns, stream);
 }
 
 // Debug builds: read (and optionally clear) this file's device-side check record.

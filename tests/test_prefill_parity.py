@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from parity_utils import compare, oracle_full, to64
 
 pytestmark = pytest.mark.gpu
@@ -155,3 +156,22 @@ def test_workload_b1h32_n8192_d64_causal(fa):
     compare(o, lse, o_ref, lse_ref, what=w.name)
     # causal row 0 sees only key 0: its output is exactly v_0
     assert torch.equal(o[:, :, 0], v[:, :, 0])
+
+
+def test_one_tile_items_in_the_last_round(fa):
+    # one 256-row unit per head and one head more than SMs: the last round's unit is taken one
+    # query tile at a time by two CTAs (and the B1 H8 N1024 and B4 H16 N2048 workloads, whose units
+    # do not fill the GPU or leave a half-empty last round, take the same path); every row of the
+    # last heads and sampled rows of the others against the oracle
+    from parity_utils import oracle_rows
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, N, d = 1, sms + 1, 256, 64
+    q, k, v, _ = _gen(B, H, N, N, d, seed=81)
+    o, lse = fa.fattn_fwd(q, k, v, scale=0.125)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(to64(q[:, -2:]), to64(k[:, -2:]), to64(v[:, -2:]), scale=0.125)
+    compare(o[:, -2:], lse[:, -2:], o_ref, lse_ref, what="last round in one-tile items")
+    rows = np.arange(0, (H - 2) * N, 997)
+    o_s, l_s = oracle_rows(q, k, v, rows, False, 0.125)
+    assert np.abs(to64(o).reshape(-1, d)[rows] - o_s).max() <= 2e-2
+    assert np.abs(to64(lse).reshape(-1)[rows] - l_s).max() <= 1e-3
