@@ -46,6 +46,7 @@ PREFILL_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "pre
 DECODE_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "decode_sm103a.cu")
 PREFILL_FP8_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "prefill_fp8_sm103a.cu")
 BACKWARD_KERNEL_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "backward_sm103a.cu")
+UNFUSED_SRC = os.path.join(ROOT, "exact_attention_31_gb300", "csrc", "unfused_sm103a.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -148,7 +149,8 @@ def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, or None when the kernel source has
     changed since the counters were taken.  Lines: `<kernel> <source-sha16> <bytes_per_launch>`."""
     src = {"prefill": PREFILL_KERNEL_SRC, "decode": DECODE_KERNEL_SRC, "backward64": BACKWARD_KERNEL_SRC,
-           "backward128": BACKWARD_KERNEL_SRC, "fp8": PREFILL_FP8_KERNEL_SRC, "fp8_64": PREFILL_FP8_KERNEL_SRC}[kernel]
+           "backward128": BACKWARD_KERNEL_SRC, "fp8": PREFILL_FP8_KERNEL_SRC, "fp8_64": PREFILL_FP8_KERNEL_SRC,
+           "unfused": UNFUSED_SRC}[kernel]
     try:
         digest = source_digest(src)
         with open(TRAFFIC_FILE) as f:
@@ -564,6 +566,7 @@ def run_ours(args):
         line["prefill_rising_scores"] = measure_rising_scores(fa, dev, stream, P, pre_avg, peaks)
     if args.configs and do_prefill and window is None and rank == 0:
         line["prefill_block_sparse_mask"] = measure_block_sparse(fa, dev, stream, P, q, k, v, o, lse, peaks)
+        line["prefill_unfused_baseline"] = measure_unfused(fa, dev, stream, P, q, k, v, pre_avg, peaks)
     if args.cpu_budget > 0:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if e2e is not None:
@@ -900,6 +903,88 @@ def measure_block_sparse(fa, dev, stream, P, q, k, v, o, lse, peaks, iters=10):
             "frac": round(tf / peaks["bf16_tflops"], 4)}
 
 
+def measure_unfused(fa, dev, stream, P, q, k, v, fused_ms, peaks, iters=10):
+    """The same prefill computed as standard attention in three kernels (fattn_fwd_unfused: a cuBLAS
+    GEMM writing S in fp32, the softmax kernel writing P in bf16, a cuBLAS GEMM for O), with the L2
+    flushed before each call as for the fused launch.  Outside the benchmark's timed region; the
+    comparison the pages' memory-traffic argument is about."""
+    import torch
+    B, H, N, d = P["B"], P["H"], P["N"], P["d"]
+    ws = torch.empty(fa.fattn_unfused_workspace_size(B, H, N, N), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale = 1 / math.sqrt(d)
+    for _ in range(3):
+        fa.fattn_fwd_unfused(q, k, v, causal=True, scale=scale, out=o, lse=lse, workspace=ws, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fa.fattn_fwd_unfused(q, k, v, causal=True, scale=scale, out=o, lse=lse, workspace=ws, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / iters
+    fl = prefill_flops(B, H, N, d, True)
+    ub = traffic.unfused_forward_bytes(B, H, N, N, d)
+    fb = prefill_bytes(B, H, N, d)
+    del ws
+    return {"workload": f"prefill_b{B}h{H}_n{N}_d{d} causal as standard attention in three kernels "
+                        "(cuBLAS GEMM -> S fp32, unfused_softmax_kernel -> P bf16 and L, cuBLAS GEMM -> O)",
+            "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+            "time_vs_fused": round(ms / fused_ms, 2),
+            "algorithmic_bytes": ub, "algorithmic_bytes_fused": fb, "bytes_vs_fused": round(ub / fb, 1),
+            "achieved_gbs_of_algorithmic_bytes": round(ub / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(ub / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "traffic_unfused_kernels": recorded_traffic("unfused") if H == 32 else None}
+
+
+def run_unfused(args):
+    """The fused prefill and the three-kernel standard attention on the prefill workload's shape, one
+    after the other (for the ncu capture of their DRAM traffic; --prefill-heads shrinks it)."""
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_31_gb300 as fa
+    from exact_attention_31_gb300.workloads import make_qkv
+    fa.lib()
+    P = dict(PREFILL, H=args.prefill_heads or PREFILL["H"])
+    B, H, N, d = P["B"], P["H"], P["N"], P["d"]
+    stream = torch.cuda.current_stream(dev)
+    q, k, v, _ = make_qkv(B, H, N, N, d, 0xFA77E000 + 4, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale = 1 / math.sqrt(d)
+    for _ in range(args.warmup):
+        fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fa.fattn_fwd(q, k, v, causal=True, scale=scale, out=o, lse=lse, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if fa.fattn_last_error() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout")
+    fused_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
+    peaks, peak_src = load_peaks()
+    un = measure_unfused(fa, dev, stream, P, q, k, v, fused_ms, peaks, iters=args.steps)
+    if rank != 0:
+        return
+    fl = prefill_flops(B, H, N, d, True)
+    line = {"metric": "prefill ms, fused (fattn_fwd) against standard attention in three kernels (fattn_fwd_unfused)",
+            "value": un["ms"], "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": False, "dtype": "bf16", "data": "synthetic: seeded iid N(0,1) rounded to bf16",
+            "config": {"workload": f"prefill_b{B}h{H}_n{N}_d{d} causal",
+                       "l2": "a 512 MiB buffer is written before every call (outside the per-call events)"},
+            "fused": {"ms": round(fused_ms, 4), "tflops": round(fl / (fused_ms * 1e-3) / 1e12, 2),
+                      "algorithmic_bytes": prefill_bytes(B, H, N, d)},
+            "unfused": un, "peak_source": peak_src}
+    print(json.dumps(line), flush=True)
+
+
 def run_e2e(fa, dev, stream, args, q, k, v, dq, dk, dv, scale_p, scale_d):
     """The same calls fed from pinned host buffers, copies included in the timing."""
     import torch
@@ -1006,9 +1091,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["both", "prefill", "decode", "backward", "fp8"], default="both",
+    ap.add_argument("--workload", choices=["both", "prefill", "decode", "backward", "fp8", "unfused"],
+                    default="both",
                     help="both = the benchmark step; prefill/decode time one half (profiling); backward "
-                         "times fattn_bwd on the prefill shape (a line of its own)")
+                         "times fattn_bwd on the prefill shape (a line of its own); unfused times the fused "
+                         "prefill and the three-kernel standard attention on that shape")
     ap.add_argument("--bwd-d", type=int, default=0, help="override d of the backward workload (64 or 128)")
     ap.add_argument("--fp8-d", type=int, default=0, help="d of the fp8 workload (64 or 128; default 128)")
     ap.add_argument("--window", type=int, default=-1,
@@ -1034,6 +1121,8 @@ def main(argv=None):
         run_backward(args)
     elif args.workload == "fp8":
         run_fp8(args)
+    elif args.workload == "unfused":
+        run_unfused(args)
     else:
         run_ours(args)
 

@@ -10,6 +10,11 @@ other implementation behind these names: if the library is missing, every call r
 With FATTN_DEBUG=1 in the environment when this module is imported, the same calls go to
 ``libfattn_debug.so``, the build whose kernels check their TMA, tensor-memory and barrier operands
 and their output stores on the device (``fattn_debug_take`` reads what they found).
+
+``fattn_fwd_unfused`` is the standard three-kernel attention (``include/fattn_unfused.h``, in
+``libfattn_unfused.so``): two cuBLAS GEMMs around a softmax kernel, with the score and probability
+matrices in device memory.  It is the baseline the fused forward's memory traffic is measured
+against, not a path the fused entry points take.
 """
 
 from __future__ import annotations
@@ -39,13 +44,18 @@ __all__ = [
     "fattn_status_string",
     "fattn_debug_build",
     "fattn_debug_take",
+    "fattn_fwd_unfused",
+    "fattn_unfused_workspace_size",
     "lib",
+    "unfused_lib",
     "LIB_PATH",
+    "UNFUSED_LIB_PATH",
 ]
 
 RELEASE_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn.so")
 DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn_debug.so")
 LIB_PATH = DEBUG_LIB_PATH if os.environ.get("FATTN_DEBUG") == "1" else RELEASE_LIB_PATH
+UNFUSED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfattn_unfused.so")
 
 FATTN_OK = 0
 FATTN_ERR_INVALID_ARG = 1
@@ -55,6 +65,7 @@ FATTN_ERR_TIMEOUT = 4
 FATTN_ERR_DEBUG = 5
 
 _lib = None
+_unfused_lib = None
 
 
 class FattnError(RuntimeError):
@@ -232,6 +243,61 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
                          1 if causal else 0, float(scale), _stream_handle(stream, q.device))
     if st != FATTN_OK:
         raise FattnError(st, "fattn_fwd")
+    return out, lse
+
+
+def unfused_lib() -> ctypes.CDLL:
+    """The loaded libfattn_unfused (raises if it has not been built)."""
+    global _unfused_lib
+    if _unfused_lib is not None:
+        return _unfused_lib
+    if not os.path.exists(UNFUSED_LIB_PATH):
+        raise RuntimeError(f"{UNFUSED_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                           "g.build()'`")
+    L = ctypes.CDLL(UNFUSED_LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fattn_unfused_workspace_size.argtypes = [i, i, i, i]
+    L.fattn_unfused_workspace_size.restype = sz
+    L.fattn_fwd_unfused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]
+    L.fattn_fwd_unfused.restype = i
+    _unfused_lib = L
+    return L
+
+
+def fattn_unfused_workspace_size(B: int, H: int, Nq: int, Nk: int) -> int:
+    return unfused_lib().fattn_unfused_workspace_size(int(B), int(H), int(Nq), int(Nk))
+
+
+def fattn_fwd_unfused(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                      workspace=None, stream=None):
+    """Standard attention in three kernels (S = scale Q K^T to device memory in fp32, a row softmax
+    writing P in bf16 and L, O = P V), the baseline of the fused forward.  Same arguments and result
+    as fattn_fwd without a band or element mask; ``workspace`` a CUDA uint8 tensor of
+    fattn_unfused_workspace_size bytes (allocated here if omitted).  Returns (out, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError(f"expected q [B,H,Nq,d], k/v [B,H,Nk,d]; got {tuple(q.shape)}, {tuple(k.shape)}, {tuple(v.shape)}")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q and k/v disagree on B, H or d")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check(lse, "lse", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(fattn_unfused_workspace_size(B, H, Nq, Nk), dtype=torch.uint8, device=q.device)
+    st = unfused_lib().fattn_fwd_unfused(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                         B, H, Nq, Nk, d, 1 if causal else 0, float(scale), workspace.data_ptr(),
+                                         workspace.numel(), _stream_handle(stream, q.device))
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_fwd_unfused")
     return out, lse
 
 

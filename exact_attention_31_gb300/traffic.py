@@ -182,6 +182,20 @@ def backward_bytes(B: int, H: int, Nq: int, Nk: int, d: int, elem_bytes: int = B
     return B * H * ((Nq * d * 3 + Nk * d * 2) * elem_bytes + Nq * FP32 + (Nq + 2 * Nk) * d * elem_bytes)
 
 
+def unfused_forward_bytes(B: int, H: int, Nq: int, Nk: int, d: int, s_bytes: int = FP32, p_bytes: int = BF16,
+                          elem_bytes: int = BF16, with_lse: bool = True) -> float:
+    """Compulsory traffic of standard attention in three kernels (the standard count of "Where the
+    time actually goes", per head): the first product reads Q and K and writes S, the softmax reads S
+    and writes P (and L), the second product reads P and V and writes O.  S and P take `s_bytes` and
+    `p_bytes` per element, the inputs and O `elem_bytes`.  With 4 bytes everywhere, n = Nq = Nk and
+    no L this is the page's 4 n^2 + 4 n d elements."""
+    per_head = float((Nq + Nk) * d * elem_bytes)  # Q, K into S = Q K^T
+    per_head += 2.0 * Nq * Nk * s_bytes           # S written, S read by the softmax
+    per_head += 2.0 * Nq * Nk * p_bytes           # P written, P read by O = P V
+    per_head += (Nk + Nq) * d * elem_bytes        # V read, O written
+    return B * H * (per_head + (Nq * FP32 if with_lse else 0))
+
+
 def forward_flops(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool) -> float:
     """The benchmark convention: 4 B H Nq Nk d, halved under the causal mask."""
     f = 4.0 * B * H * Nq * Nk * d

@@ -137,3 +137,16 @@ def test_benchmark_algorithmic_bytes():
     assert T.fused_forward_reread_bytes(1, 1, 8192, 8192, 64, Br=256, window_right=0) > \
         4 * T.fused_forward_bytes(1, 1, 8192, 8192, 64)
     assert T.forward_flops(1, 32, 8192, 8192, 64, True) == 274877906944.0
+
+
+def test_unfused_kernels_count_is_the_standard_count():
+    # the three-kernel baseline's byte count, with every element in 4 bytes and no L, is the page's
+    # standard column; with the library's types (S fp32, P bf16, bf16 tensors) it is what the
+    # benchmark divides the unfused time by
+    for r in TABLES["Where the time actually goes"]["rows"]:
+        n = int(r["n"])
+        b = T.unfused_forward_bytes(1, 1, n, n, D, s_bytes=4, p_bytes=4, elem_bytes=4, with_lse=False)
+        assert F(b / T.MIB, 2) == r["hbm_mb"], n
+    n, d = 8192, 64
+    assert T.unfused_forward_bytes(1, 32, n, n, d) == 32 * (2 * n * d * 2 + 2 * n * n * 4 + 2 * n * n * 2
+                                                            + 2 * n * d * 2 + 4 * n)
