@@ -562,6 +562,15 @@ struct BMma {
     for (int kk = 0; kk < kBN / 16; ++kk)
       mma_ss_lead(tmem + C::col_dq(b), aa + mn_adv(kk), k_mn + mn_adv(kk), id, kk > 0 ? 1u : 0u, lead);
   }
+  // dQ columns [64 h, 64 h + 64) only (d = 128): the drain's first pass starts while the second half
+  // is still being computed.
+  __device__ __forceinline__ void issue_dq_half(int dsb, int h) const {
+    constexpr uint32_t id = mma_idesc_bf16_f32(kBM, 64, true, true);
+    const uint64_t aa = ds_mn0 + ds_adv(dsb), bk = k_mn + static_cast<uint64_t>(h * kAtom >> 4);
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+      mma_ss_lead(tmem + C::kColDP + 64 * h, aa + mn_adv(kk), bk + mn_adv(kk), id, kk > 0 ? 1u : 0u, lead);
+  }
   __device__ __forceinline__ void commit(int bar) const { mma_commit_lead(sbar + 8 * bar, lead); }
   __device__ __forceinline__ bool wait(int bar, int parity, const Abort& ab) const {
     return warp_wait(sbar + 8 * bar, parity & 1, ab);
@@ -647,8 +656,11 @@ __device__ __forceinline__ bool mma_schedule_one(int n, const BMma<D>& m, const 
     m.commit(C::kQEmpty);
     m.issue_dv(0, 0, i == 0);
     m.commit(C::kOEmpty);
-    m.issue_dq(0, dsb);  // into the dP^T columns, read by the compute warps already
+    // dQ_i into the dP^T columns (read by the compute warps already), in two halves of 64 columns
+    m.issue_dq_half(dsb, 0);
     m.commit(C::kDQFull);
+    m.issue_dq_half(dsb, 1);
+    m.commit(C::kDQFull + 1);
     m.commit(C::kDSEmpty + dsb);
     if (i + 1 < n) {
       // S^T of the next tile after dV_i has read P^T from the same columns (issue order).
@@ -709,12 +721,17 @@ __device__ __forceinline__ void drain_role(const CUtensorMap* tdq, int n, int it
   for (int i = 0; i < n; ++i) {
     const int b = i % C::kSBufs;
     if constexpr (M) qt = next_qtile<M>(a, bits, qt);
-    bool fail = !warp_wait(sbar + 8 * (C::kDQFull + b), (i / C::kSBufs) & 1, ab);
-    if (!fail) tc_fence_after();
+    // d = 64: one dQ buffer per tile; d = 128: dQ in two 64-column halves, one per pass
+    bool fail = C::kTwoS && !warp_wait(sbar + 8 * (C::kDQFull + b), (i / C::kSBufs) & 1, ab);
+    if (C::kTwoS && !fail) tc_fence_after();
     const int q0 = (M ? qt : it0 + i) * kBM;
 #pragma unroll 1
     for (int pass = 0; pass < D / 64; ++pass) {
       uint32_t v[2][32];
+      if (!C::kTwoS && !fail) {
+        fail = !warp_wait(sbar + 8 * (C::kDQFull + pass), i & 1, ab);
+        if (!fail) tc_fence_after();
+      }
       if (!fail) {
         const uint32_t t = tmem + lane_field + C::col_dq(b) + 64 * pass;
         tmem_ld_32x32b_x32(t, v[0]);
