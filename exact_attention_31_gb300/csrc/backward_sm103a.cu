@@ -82,28 +82,39 @@ template <int D>
 struct BCfg {
   static constexpr bool kTwoS = (D == 64);
   static constexpr int kSBufs = kTwoS ? 2 : 1;
-  static constexpr int kStages = kTwoS ? 2 : 1;   // Q_i/dO_i buffers (d = 64: two measured 2 % faster than three)
+  // Q_i and dO_i buffers: d = 64 two Q and three dO (the dO reload is on the path to the next dP^T),
+  // d = 128 one of each.
+  static constexpr int kQStages = kTwoS ? 2 : 1;
+  static constexpr int kOStages = kTwoS ? 3 : 1;
   static constexpr int kDSBufs = 1;               // dS^T buffers
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kTile = kBM * D * 2;  // one 128-row bf16 tile of Q, K, V or dO
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kTile;
-  static constexpr uint32_t kStageOff = 2 * kTile;  // stage s: Q at + 2*s*kTile, dO at + (2s+1)*kTile
+  static constexpr uint32_t kStageOff = 2 * kTile;  // Q stages, then dO stages
+  __host__ __device__ static constexpr uint32_t q_off(int st) { return kStageOff + static_cast<uint32_t>(st) * kTile; }
+  __host__ __device__ static constexpr uint32_t do_off(int st) {
+    return kStageOff + static_cast<uint32_t>(kQStages + st) * kTile;
+  }
   static constexpr uint32_t kDSBytes = kBN * kBM * 2;
-  static constexpr uint32_t kDSOff = kStageOff + kStages * 2 * kTile;
+  static constexpr uint32_t kDSOff = kStageOff + (kQStages + kOStages) * kTile;
   static constexpr uint32_t kDQOff = kDSOff + kDSBufs * kDSBytes;  // 64 columns of dQ at a time
   static constexpr uint32_t kDQBytes = kBM * 64 * 4;
   static constexpr uint32_t kOnesOff = kDQOff + kDQBytes;  // [128 rows][16] bf16 of the constant A block
   static constexpr uint32_t kExtBytes = kBM * 32;             // [128 rows][16] bf16
-  static constexpr uint32_t kExtOff = kOnesOff + kExtBytes;   // stage s: Q terms at + 2*s*kExtBytes, dO terms after
-  static constexpr uint32_t kBarOff = kExtOff + kStages * 2 * kExtBytes;
+  static constexpr uint32_t kExtOff = kOnesOff + kExtBytes;   // Q terms per Q stage, then dO terms per dO stage
+  __host__ __device__ static constexpr uint32_t ext_q_off(int st) { return kExtOff + static_cast<uint32_t>(st) * kExtBytes; }
+  __host__ __device__ static constexpr uint32_t ext_do_off(int st) {
+    return kExtOff + static_cast<uint32_t>(kQStages + st) * kExtBytes;
+  }
+  static constexpr uint32_t kBarOff = kExtOff + (kQStages + kOStages) * kExtBytes;
   // barrier indices
-  static_assert(kStages <= 4, "barrier slots");
+  static_assert(kQStages <= 4 && kOStages <= 4, "barrier slots");
   static constexpr int kKVFull = 0;
-  static constexpr int kQFull = 1;     // [kStages] Q_i and its extra K-step block landed
-  static constexpr int kOFull = 5;     // [kStages] dO_i and its extra K-step block landed
-  static constexpr int kQEmpty = 9;    // [kStages] Q_i's last reader (dK_i) done
-  static constexpr int kOEmpty = 13;   // [kStages] dO_i's last reader (dV_i) done
+  static constexpr int kQFull = 1;     // [kQStages] Q_i and its extra K-step block landed
+  static constexpr int kOFull = 5;     // [kOStages] dO_i and its extra K-step block landed
+  static constexpr int kQEmpty = 9;    // [kQStages] Q_i's last reader (dK_i) done
+  static constexpr int kOEmpty = 13;   // [kOStages] dO_i's last reader (dV_i) done
   static constexpr int kSFull = 17;    // [2] S^T of a buffer computed
   static constexpr int kDPFull = 19;   // dP^T computed
   static constexpr int kCDone = 20;    // compute warps done with a tile (one arrival per warp)
@@ -438,34 +449,37 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tq, const CUten
   int qt = it0 - 1;  // element mask: the query tile of step i
   const unsigned long long* bits = M ? key_tile_bits(a, bh, n0 / kBN) : nullptr;
   for (int i = 0; i < n && ok; ++i) {
-    const int st = i % C::kStages, use = i / C::kStages;
     if constexpr (M) qt = next_qtile<M>(a, bits, qt);
     const int q0 = (M ? qt : it0 + i) * kBM;
     const size_t r0 = (static_cast<size_t>(bh) * a.Nq_pad + q0) * 16;
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
+      const int stages = w ? C::kOStages : C::kQStages;
+      const int st = i % stages, use = i / stages;
       if (use > 0 && !thread_wait(sbar + 8 * ((w ? C::kOEmpty : C::kQEmpty) + st), (use - 1) & 1, ab)) {
         ok = false;
         break;
       }
       const uint32_t bar = sbar + 8 * ((w ? C::kOFull : C::kQFull) + st);
-      const uint32_t dst = sbase + C::kStageOff + (2 * st + w) * C::kTile;
+      const uint32_t dst = sbase + (w ? C::do_off(st) : C::q_off(st));
       mbar_arrive_expect_tx(bar, C::kTile + C::kExtBytes);
 #pragma unroll
       for (int ch = 0; ch < C::kChunks; ++ch) tma_load_3d(dst + ch * kAtom, w ? tdo : tq, bar, 64 * ch, q0, bh);
-      bulk_load(sbase + C::kExtOff + (2 * st + w) * C::kExtBytes, (w ? a.ext_do : a.ext_q) + r0, C::kExtBytes, bar);
+      bulk_load(sbase + (w ? C::ext_do_off(st) : C::ext_q_off(st)), (w ? a.ext_do : a.ext_q) + r0, C::kExtBytes, bar);
       issued = 2 * i + w + 1;
     }
   }
   if (!ok) {
-    // Let the copies already in flight land before the CTA's shared memory goes away.
+    // Let the copies already in flight land before the CTA's shared memory goes away: the last
+    // loads of each kind, as many as it has buffers.
     const uint64_t until = globaltimer_ns() + 50ull * 1000 * 1000;
     volatile uint32_t never = 0;
     if (!a.drop_kv) mbar_wait_bounded(sbar + 8 * C::kKVFull, 0, &never, until);
-    for (int idx = max(0, issued - 2 * C::kStages); idx < issued; ++idx) {
+    for (int idx = max(0, issued - 2 * max(C::kQStages, C::kOStages)); idx < issued; ++idx) {
       const int i = idx >> 1, w = idx & 1;
-      mbar_wait_bounded(sbar + 8 * ((w ? C::kOFull : C::kQFull) + i % C::kStages), (i / C::kStages) & 1, &never,
-                        until);
+      const int stages = w ? C::kOStages : C::kQStages;
+      if (i < (issued - 1 - w) / 2 + 1 - stages) continue;  // an older load of a buffer reused since
+      mbar_wait_bounded(sbar + 8 * ((w ? C::kOFull : C::kQFull) + i % stages), (i / stages) & 1, &never, until);
     }
   }
 }
@@ -490,50 +504,56 @@ struct BMma {
     k_kmaj = smem_desc_sw128(sbase + C::kKOff, 16, 1024);
     v_kmaj = smem_desc_sw128(sbase + C::kVOff, 16, 1024);
     k_mn = smem_desc_sw128(sbase + C::kKOff, kAtom, 1024);
-    q_kmaj0 = smem_desc_sw128(sbase + C::kStageOff, 16, 1024);
-    do_kmaj0 = smem_desc_sw128(sbase + C::kStageOff + C::kTile, 16, 1024);
-    q_mn0 = smem_desc_sw128(sbase + C::kStageOff, kAtom, 1024);
-    do_mn0 = smem_desc_sw128(sbase + C::kStageOff + C::kTile, kAtom, 1024);
+    q_kmaj0 = smem_desc_sw128(sbase + C::q_off(0), 16, 1024);
+    do_kmaj0 = smem_desc_sw128(sbase + C::do_off(0), 16, 1024);
+    q_mn0 = smem_desc_sw128(sbase + C::q_off(0), kAtom, 1024);
+    do_mn0 = smem_desc_sw128(sbase + C::do_off(0), kAtom, 1024);
     ds_kmaj0 = smem_desc_sw128(sbase + C::kDSOff, 16, 1024);
     ds_mn0 = smem_desc_sw128(sbase + C::kDSOff, kAtom, 1024);
     ones = smem_desc_sw32(sbase + C::kOnesOff);
-    ext_q0 = smem_desc_sw32(sbase + C::kExtOff);
-    ext_do0 = smem_desc_sw32(sbase + C::kExtOff + C::kExtBytes);
+    ext_q0 = smem_desc_sw32(sbase + C::ext_q_off(0));
+    ext_do0 = smem_desc_sw32(sbase + C::ext_do_off(0));
     lead = elect_lane();
   }
   // start-address advances, in 16-byte units
-  __host__ __device__ static constexpr uint64_t stage_adv(int st) { return static_cast<uint64_t>(st) * (2 * C::kTile >> 4); }
+  __host__ __device__ static constexpr uint64_t q_adv(int st) { return static_cast<uint64_t>(C::q_off(st) - C::q_off(0)) >> 4; }
+  __host__ __device__ static constexpr uint64_t do_adv(int st) { return static_cast<uint64_t>(C::do_off(st) - C::do_off(0)) >> 4; }
   __host__ __device__ static constexpr uint64_t ds_adv(int b) { return static_cast<uint64_t>(b) * (C::kDSBytes >> 4); }
   // K-major operand, K step kk of 16 elements: 4 steps per 128-byte row, then the next 64-column chunk
   __host__ __device__ static constexpr uint64_t kmaj_adv(int kk) { return static_cast<uint64_t>((kk >> 2) * kAtom + (kk & 3) * 32) >> 4; }
   // MN-major operand, K step kk of 16 rows
   __host__ __device__ static constexpr uint64_t mn_adv(int kk) { return static_cast<uint64_t>(kk * 16 * 128) >> 4; }
 
-  __host__ __device__ static constexpr uint64_t ext_adv(int st) { return static_cast<uint64_t>(st) * (2 * C::kExtBytes >> 4); }
+  __host__ __device__ static constexpr uint64_t ext_q_adv(int st) {
+    return static_cast<uint64_t>(C::ext_q_off(st) - C::ext_q_off(0)) >> 4;
+  }
+  __host__ __device__ static constexpr uint64_t ext_do_adv(int st) {
+    return static_cast<uint64_t>(C::ext_do_off(st) - C::ext_do_off(0)) >> 4;
+  }
   // S'^T = K Q^T + ones (terms of -L / scale)^T
   __device__ __forceinline__ void issue_s(int b, int st) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM, false);
-    const uint64_t bq = q_kmaj0 + stage_adv(st);
+    const uint64_t bq = q_kmaj0 + q_adv(st);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_lead(tmem + C::col_s(b), k_kmaj + kmaj_adv(kk), bq + kmaj_adv(kk), id, kk > 0 ? 1u : 0u, lead);
-    mma_ss_lead(tmem + C::col_s(b), ones, ext_q0 + ext_adv(st), id, 1u, lead);
+    mma_ss_lead(tmem + C::col_s(b), ones, ext_q0 + ext_q_adv(st), id, 1u, lead);
   }
   // dP'^T = V dO^T + ones (terms of -D)^T
   __device__ __forceinline__ void issue_dp(int st) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM, false);
-    const uint64_t bd = do_kmaj0 + stage_adv(st);
+    const uint64_t bd = do_kmaj0 + do_adv(st);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_lead(tmem + C::kColDP, v_kmaj + kmaj_adv(kk), bd + kmaj_adv(kk), id, kk > 0 ? 1u : 0u, lead);
-    mma_ss_lead(tmem + C::kColDP, ones, ext_do0 + ext_adv(st), id, 1u, lead);
+    mma_ss_lead(tmem + C::kColDP, ones, ext_do0 + ext_do_adv(st), id, 1u, lead);
   }
   // dP'^T of queries [64 h, 64 h + 64) only, into those 64 columns (N = 64): d = 128, where each half
   // goes as soon as the drain warps have read the dQ columns under it.
   __device__ __forceinline__ void issue_dp_half(int st, int h) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, kBM / 2, false);
-    const uint64_t bd = do_kmaj0 + stage_adv(st) + static_cast<uint64_t>(h * (kBM / 2) * 128 >> 4);
-    const uint64_t be = ext_do0 + ext_adv(st) + static_cast<uint64_t>(h * (kBM / 2) * 32 >> 4);
+    const uint64_t bd = do_kmaj0 + do_adv(st) + static_cast<uint64_t>(h * (kBM / 2) * 128 >> 4);
+    const uint64_t be = ext_do0 + ext_do_adv(st) + static_cast<uint64_t>(h * (kBM / 2) * 32 >> 4);
     const uint32_t dcol = tmem + C::kColDP + (kBM / 2) * h;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
@@ -542,7 +562,7 @@ struct BMma {
   }
   __device__ __forceinline__ void issue_dv(int b, int st, bool first) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, D, true);
-    const uint64_t bd = do_mn0 + stage_adv(st);
+    const uint64_t bd = do_mn0 + do_adv(st);
 #pragma unroll
     for (int kk = 0; kk < kBM / 16; ++kk)
       mma_ts_lead(tmem + C::kColDV, tmem + C::col_s(b) + p_step_col(kk), bd + mn_adv(kk), id,
@@ -550,7 +570,7 @@ struct BMma {
   }
   __device__ __forceinline__ void issue_dk(int dsb, int st, bool first) const {
     constexpr uint32_t id = mma_idesc_bf16_f32(kBN, D, true);
-    const uint64_t aa = ds_kmaj0 + ds_adv(dsb), bq = q_mn0 + stage_adv(st);
+    const uint64_t aa = ds_kmaj0 + ds_adv(dsb), bq = q_mn0 + q_adv(st);
 #pragma unroll
     for (int kk = 0; kk < kBM / 16; ++kk)
       mma_ss_lead(tmem + C::kColDK, aa + kmaj_adv(kk), bq + mn_adv(kk), id, (!first || kk > 0) ? 1u : 0u, lead);
@@ -587,25 +607,25 @@ __device__ __forceinline__ bool mma_schedule_two(int n, const BMma<D>& m, const 
   m.issue_dp(0);
   m.commit(C::kDPFull);
   for (int i = 0; i < n; ++i) {
-    const int b = i & 1, st = i % C::kStages, dsb = i % C::kDSBufs;
+    const int b = i & 1, qs = i % C::kQStages, os = i % C::kOStages, dsb = i % C::kDSBufs;
     if (i + 1 < n) {
-      if (!m.wait(C::kDPFree, i, ab) || !m.wait(C::kOFull + (i + 1) % C::kStages, (i + 1) / C::kStages, ab))
+      if (!m.wait(C::kDPFree, i, ab) || !m.wait(C::kOFull + (i + 1) % C::kOStages, (i + 1) / C::kOStages, ab))
         return false;
       tc_fence_after();
-      m.issue_dp((i + 1) % C::kStages);
+      m.issue_dp((i + 1) % C::kOStages);
       m.commit(C::kDPFull);
     }
     if (!m.wait(C::kCDone, i, ab)) return false;
     tc_fence_after();
     // dK_i and dQ_i first: they release the one dS^T buffer, which the compute warps of tile i+1
     // are about to refill; then dV_i.  (Measured: 2 % faster than dV, dK, dQ with three Q/dO stages.)
-    m.issue_dk(dsb, st, i == 0);
-    m.commit(C::kQEmpty + st);
+    m.issue_dk(dsb, qs, i == 0);
+    m.commit(C::kQEmpty + qs);
     m.issue_dq(b, dsb);
     m.commit(C::kDQFull + b);
     m.commit(C::kDSEmpty + dsb);
-    m.issue_dv(b, st, i == 0);
-    m.commit(C::kOEmpty + st);
+    m.issue_dv(b, os, i == 0);
+    m.commit(C::kOEmpty + os);
   }
   m.commit(C::kAccDone);
   return true;
@@ -622,12 +642,12 @@ __device__ __forceinline__ bool mma_schedule_s(int n, const BMma<D>& m, const Ab
     const int b = t & 1;
     if (t >= 2) {
       const int u = t - 2;
-      if (!m.wait(C::kDQFree + b, u / 2, ab) || !m.wait(C::kOEmpty + u % C::kStages, u / C::kStages, ab))
+      if (!m.wait(C::kDQFree + b, u / 2, ab) || !m.wait(C::kOEmpty + u % C::kOStages, u / C::kOStages, ab))
         return false;
     }
-    if (!m.wait(C::kQFull + t % C::kStages, t / C::kStages, ab)) return false;
+    if (!m.wait(C::kQFull + t % C::kQStages, t / C::kQStages, ab)) return false;
     tc_fence_after();
-    m.issue_s(b, t % C::kStages);
+    m.issue_s(b, t % C::kQStages);
     m.commit(C::kSFull + b);
   }
   return true;
@@ -817,10 +837,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(sbar + 8 * C::kKVFull, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(sbar + 8 * (C::kQFull + s), 1);
-      mbar_init(sbar + 8 * (C::kOFull + s), 1);
       mbar_init(sbar + 8 * (C::kQEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kOStages; ++s) {
+      mbar_init(sbar + 8 * (C::kOFull + s), 1);
       mbar_init(sbar + 8 * (C::kOEmpty + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
