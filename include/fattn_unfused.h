@@ -50,8 +50,8 @@ size_t fattn_unfused_workspace_size(int B, int H, int Nq, int Nk);
  *   3. O = P V, a cuBLAS bf16 GEMM that writes O in bf16.
  *
  * The first call on a device creates that device's cuBLAS handle and a 32 MiB cuBLAS workspace and
- * keeps them for the life of the process; later calls allocate nothing and may be captured in a
- * CUDA graph.  Returns FATTN_ERR_INVALID_ARG or FATTN_ERR_UNSUPPORTED for rejected arguments (nothing
+ * keeps them for the life of the process; later calls allocate no device memory.  (Capture of these
+ * calls in a CUDA graph is not covered by the tests.)  Returns FATTN_ERR_INVALID_ARG or FATTN_ERR_UNSUPPORTED for rejected arguments (nothing
  * launched) and FATTN_ERR_CUDA when cuBLAS or the runtime refuses a call.
  */
 fattn_status fattn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
